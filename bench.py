@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark: GDN verify + greedy accept + on-device restore, one GPU.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch: gdn_verify_span over
+every layer (with per-token F32 checkpoints), spec_accept_greedy over the
+logits, gdn_rollback_restore of the accepted slot. Default workload: 48 GDN
+layers (H_k=16, H_v=32, d=128, 8192 channels, conv 4), chain span 16,
+batch 1, logits [17, 151936] (synthetic, seeded). Metric: verified
+tokens x layers per second.
+
+Timing: W untimed warm-up steps, then exactly K timed steps between a barrier
++ synchronize on both sides. Each step is bracketed by CUDA events on the
+launching stream; a 256 MiB buffer (larger than the 129 MB L2) is written
+between steps, outside the events. The verify kernel's own events give the
+roofline line. For N > 1 (torchrun) every rank runs its own requests
+(replicas, no data-path collective); the step time is the max over ranks and
+the value sums the units of all ranks.
+
+--impl reference times the CPU oracle (plain C, double precision, one
+thread) on the same workload, each step a bounded sample of it (a few
+layers); it is a deliberately slow correctness program, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN verify+rollback tokens·layers/s (span 16, 48 layers); % of HBM roofline"
+UNIT = "tokens*layers/s"
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+VERIFY_SRC = os.path.join(ROOT, "speculative_decode_hybrid_gb300", "csrc", "gdn_verify.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_verify_kernel_traffic.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--seed", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per verify launch from the committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    try:
+        vals = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        with open(VERIFY_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if vals.get("source_sha256") != sha:
+            return None
+        return int(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed loop runs."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t_begin: float, t_end: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t_begin - 0.05 <= r[0] <= t_end + 0.15] or rows[-2:]
+        sm = []
+        reasons = set()
+        pw = []
+        smax = None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in inside:
+            try:
+                sm.append(float(p[2]))
+                smax = float(p[3])
+                pw.append(float(p[4]))
+            except ValueError:
+                pass
+            for n, v in zip(names, p[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max(pw) if pw else None}
+
+
+def config_of(st, wl, kl):
+    s = wl.shape
+    from speculative_decode_hybrid_gb300.workloads import WORKLOAD_NAMES
+    return {"workload": WORKLOAD_NAMES.get(BENCH_WID, "custom"), "batch": s.batch, "layers": s.layers,
+            "span": s.n_tok, "tree_nodes": s.n_nodes if s.tree else None,
+            "h_k": s.h_k, "h_v": s.h_v, "d_k": s.d_k, "d_v": s.d_v, "conv_channels": s.conv_ch,
+            "conv_k": s.conv_k, "vocab": s.vocab, "input_dtype": "bf16" if s.dtype == 1 else "f32",
+            "state_dtype": "f32", "accepted_len": [int(k) for k in kl], "seed": wl.seed,
+            "l2": "256 MiB buffer written between timed steps (outside the events); "
+                  "step footprint %.2f GiB" % (st.verify_bytes() / 2 ** 30),
+            "parallelism": "replicas (independent requests per rank, no collective)"}
+
+
+BENCH_WID = 2
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decode_hybrid_gb300 import build as B
+    from speculative_decode_hybrid_gb300 import gdnspec as G
+    from speculative_decode_hybrid_gb300 import workloads as W
+    from speculative_decode_hybrid_gb300.pipeline import SpecStep, pinned_host_inputs, run_host_step
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    G.load()
+
+    wl = W.make_workload(BENCH_WID, seed=args.seed + 1000 * rank)
+    st = SpecStep(wl, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ssm0 = st.ssm_state.clone()
+    conv0 = st.conv_state.clone()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for i in range(max(3, args.warmup)):
+        st.step()
+    torch.cuda.synchronize(dev)
+    kl = st.accept_len.cpu().numpy()
+    kn = st.accept_node.cpu().numpy()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_begin = time.time()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e = ev[i]
+        e[0].record(stream)
+        st.verify()
+        e[1].record(stream)
+        st.accept()
+        e[2].record(stream)
+        st.restore()
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_end = time.time()
+    clocks = sampler.stop(t_begin, t_end)
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    ver_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    acc_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    res_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_ms = sum(step_ms)
+    tot = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    total_max_ms = float(tot.item())
+    units = st.units()
+    value = units * K * ws / (total_max_ms / 1e3)
+
+    hbm, peak_kind = peaks()
+    vbytes = st.verify_bytes()
+    ver_mean_s = statistics.mean(ver_ms) / 1e3
+    achieved = vbytes / ver_mean_s / 1e9
+    step_bytes = vbytes + st.accept_bytes() + st.restore_bytes(kn)
+    step_gbs = step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9
+
+    # ---- end to end through the public API, host buffers, copies timed
+    host = pinned_host_inputs(wl)
+    out_host = {"accept_len": torch.empty(st.accept_len.shape, dtype=torch.int32).pin_memory(),
+                "accept_node": torch.empty(st.accept_node.shape, dtype=torch.int32).pin_memory(),
+                "argmax": torch.empty(st.argmax.shape, dtype=torch.int32).pin_memory()}
+    E = max(1, min(args.e2e_steps, K))
+    e2e_s = []
+    h2d = d2h = 0
+    for i in range(E + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        h2d, d2h = run_host_step(st, host, out_host)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        if i >= 3:
+            e2e_s.append(t1 - t0)
+    e2e_tot = torch.tensor([sum(e2e_s)], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(e2e_tot, op=dist.ReduceOp.MAX)
+    e2e_value = units * E * ws / float(e2e_tot.item())
+    assert int(out_host["accept_len"][0]) == int(kl[0])
+
+    # the state moved every step; put the initial one back (not timed)
+    st.ssm_state.copy_(ssm0)
+    st.conv_state.copy_(conv0)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": total_max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(st, wl, kl),
+        "roofline": {"bound": "hbm", "kernel": "gdn_verify_kernel (gdn_verify_span)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": peak_kind, "traffic": recorded_traffic(),
+                     "algorithmic_bytes_per_launch": vbytes,
+                     "verify_us_mean": ver_mean_s * 1e6,
+                     "verify_us_median": statistics.median(ver_ms) * 1e3,
+                     "accept_us_mean": statistics.mean(acc_ms) * 1e3,
+                     "restore_us_mean": statistics.mean(res_ms) * 1e3,
+                     "step_bytes": step_bytes, "step_gbs": step_gbs, "step_frac": step_gbs / hbm},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s)},
+        "clocks": clocks,
+        "gpu_launches": SpecStep.LAUNCHES_PER_STEP * K,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def oracle_full_step(wl, layers, accept=True):
+    """One oracle step over `layers`: verify + restore of each, plus acceptance."""
+    import oracle
+    res = oracle.verify_request(wl, 0, layers=layers)
+    par = wl.parent[0] if wl.parent is not None else None
+    kl, kn = 0, 0
+    if accept:
+        _, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0], par)
+    for y, (ck, cc, _) in zip(layers, res):
+        oracle.restore(ck, kn, wl.ssm0[0, y])
+        oracle.restore(cc, kn, wl.conv0[0, y])
+    return kl
+
+
+def cpu_baseline(wl, target_s):
+    """The oracle as it stands, single thread, on full steps of request 0."""
+    s = wl.shape
+    layers = list(range(s.layers))
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle_full_step(wl, layers)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all >= target_s or len(times) >= 30:
+            break
+    per = statistics.mean(times)
+    return {"value": s.n_tok * s.layers / per, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d full steps of request 0 (%d layers verify + accept + restore), "
+                      "plain C double precision, one thread, %.1f s total" % (len(times), s.layers,
+                                                                             sum(times))}
+
+
+def run_reference(args):
+    """The oracle on the host cores, K steps of a bounded sample each."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decode_hybrid_gb300 import workloads as W
+    oracle.build()
+    wl = W.make_workload(BENCH_WID, seed=args.seed)
+    s = wl.shape
+    # calibrate: one layer + acceptance
+    t0 = time.perf_counter()
+    oracle_full_step(wl, [0])
+    t1 = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nl = int(max(1, min(s.layers, budget // max(t1, 1e-3))))
+    # the acceptance runs once per s.layers layers of verify work, as in a full step
+    def sample(i):
+        layers = [(i * nl + j) % s.layers for j in range(nl)]
+        return layers, (i * nl) % s.layers < nl
+
+    for i in range(args.warmup):
+        oracle_full_step(wl, *sample(i))
+    times = []
+    for i in range(args.steps):
+        layers, acc = sample(i)
+        t0 = time.perf_counter()
+        oracle_full_step(wl, layers, acc)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = s.n_tok * nl * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": W.WORKLOAD_NAMES[BENCH_WID], "layers_per_step_sample": nl,
+                       "seed": wl.seed},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "each step: %d of %d layers (verify + restore); the acceptance "
+                                       "once per %d layers of work; plain C double precision, one "
+                                       "thread" % (nl, s.layers, s.layers)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    global BENCH_WID
+    args = parse()
+    BENCH_WID = args.workload
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

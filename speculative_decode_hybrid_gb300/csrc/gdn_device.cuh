@@ -1,0 +1,44 @@
+// Small device helpers of the gdnspec kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace gdndev {
+
+// Load element i of an input array stored as bf16 or f32, widened to f32
+// (bf16 -> f32 is exact).
+template <bool BF16>
+__device__ __forceinline__ float ld_in(const void *p, size_t i) {
+    if constexpr (BF16) {
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+    } else {
+        return reinterpret_cast<const float *>(p)[i];
+    }
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// 16-byte store that marks the line evict-first in L2: checkpoint slots are
+// written once and read at most once (by the restore of one slot).
+__device__ __forceinline__ void st4_stream(float *p, float4 v) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :
+                 : "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+    acc = fmaf(a.z, b.z, acc);
+    acc = fmaf(a.w, b.w, acc);
+    return acc;
+}
+
+__device__ __forceinline__ float silu(float y) { return y / (1.0f + expf(-y)); }
+
+}  // namespace gdndev

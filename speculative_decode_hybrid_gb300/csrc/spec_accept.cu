@@ -1,0 +1,204 @@
+// spec_accept_greedy: greedy acceptance of drafted chains / trees against
+// the target's argmax, on sm_103a (openinfer PR #626, Summary: the
+// speculative output must match plain greedy decoding; lucebox PR #533,
+// Changes: top-K/argmax run on the GPU's logits).
+//
+// One launch:
+//  * grid (splits, N, B): each CTA scans a contiguous, 16-byte aligned chunk
+//    of one logit row with streaming float4 loads and reduces it to one
+//    64-bit key  (order-preserving bits of the value << 32) | (~index),
+//    so a plain max picks the largest value and, among equal values, the
+//    lowest index; every NaN maps to the top value and the first NaN wins.
+//    -0.0 is folded into +0.0 so that equal values tie by index.
+//  * The CTA stores its key into the caller's workspace and bumps a
+//    per-request arrival counter. The last CTA of a request (threadfence +
+//    atomic counter, no spinning) reduces the keys of every row of that
+//    request, writes argmax_out, walks the chain or tree once and writes
+//    accept_len / accept_node, then puts the counter back to zero.
+#include <cuda_runtime.h>
+
+#include "gdn_device.cuh"
+#include "gdn_host.h"
+#include "gdnspec.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxSplits = 64;
+constexpr int kMaxNodes = GDN_MAX_TOKENS + 1;
+constexpr size_t kCounterBytes(int32_t batch) { return (((size_t)batch * 4 + 255) / 256) * 256; }
+
+__device__ __forceinline__ unsigned long long make_key(float f, unsigned idx) {
+    unsigned u = __float_as_uint(f);
+    unsigned ord;
+    if (f != f) {
+        ord = 0xFFFFFFFFu;
+    } else {
+        if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
+        ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+// Among two distinct matching nodes of equal depth: is i's root path lower
+// than j's at the first divergence?
+__device__ bool path_less(const int *par, int i, int j) {
+    for (int guard = 0; guard < kMaxNodes && par[i] != par[j]; ++guard) {
+        i = par[i];
+        j = par[j];
+    }
+    return i < j;
+}
+
+__global__ void __launch_bounds__(kThreads)
+spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict__ logits,
+                   const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
+                   int32_t *argmax_out, int32_t *accept_len, int32_t *accept_node,
+                   unsigned *counters, unsigned long long *keys, int32_t *dev_status) {
+    __shared__ unsigned long long red[kThreads / 32];
+    __shared__ bool is_last;
+    __shared__ int am_s[kMaxNodes], par_s[kMaxNodes], dep_s[kMaxNodes];
+    __shared__ unsigned char ok_s[kMaxNodes];
+
+    const int split = blockIdx.x, n = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x;
+    const float *row = logits + ((size_t)b * N + n) * (size_t)V;
+    const int lo = split * chunk;
+    const int hi = min(V, lo + chunk);
+
+    unsigned long long best = 0ull;  // below every real element
+    if ((V & 3) == 0) {
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        const int lo4 = lo >> 2, hi4 = hi >> 2;  // lo is a multiple of 4
+#pragma unroll 4
+        for (int i = lo4 + tid; i < hi4; i += kThreads) {
+            const float4 f = __ldcs(r4 + i);
+            const unsigned base = (unsigned)i * 4u;
+            best = umax64(best, make_key(f.x, base));
+            best = umax64(best, make_key(f.y, base + 1));
+            best = umax64(best, make_key(f.z, base + 2));
+            best = umax64(best, make_key(f.w, base + 3));
+        }
+    } else {
+        for (int i = lo + tid; i < hi; i += kThreads) best = umax64(best, make_key(__ldcs(row + i), (unsigned)i));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, off));
+    if ((tid & 31) == 0) red[tid >> 5] = best;
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < kThreads / 32; ++w) best = umax64(best, red[w]);
+        if ((unsigned)(best >> 32) == 0xFFFFFFFFu && dev_status) atomicOr(dev_status, GDN_DEV_NAN_LOGIT);
+        keys[((size_t)b * N + n) * splits + split] = best;
+        __threadfence();
+        const unsigned prev = atomicAdd(&counters[b], 1u);
+        is_last = prev == (unsigned)(N * splits - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    // ---- last CTA of request b: finish the argmax of every row, then walk
+    for (int r = tid; r < N; r += kThreads) {
+        unsigned long long k = 0ull;
+        const unsigned long long *kr = keys + ((size_t)b * N + r) * splits;
+        for (int s = 0; s < splits; ++s) k = umax64(k, __ldcg(kr + s));
+        const int am = (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
+        am_s[r] = am;
+        argmax_out[(size_t)b * N + r] = am;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int32_t *tok = tokens + (size_t)b * N;
+        int flags = 0;
+        int best_node = 0;
+        if (parent == nullptr) {
+            bool run = true;
+            for (int i = 1; i < N; ++i) {
+                const int t = tok[i];
+                if (t < 0 || t >= V) flags |= GDN_DEV_TOKEN_RANGE;
+                if (run && t == am_s[i - 1]) best_node = i;
+                else run = false;
+            }
+            accept_len[b] = best_node;
+        } else {
+            const int32_t *par = parent + (size_t)b * N;
+            par_s[0] = -1;
+            dep_s[0] = 0;
+            ok_s[0] = 1;
+            for (int i = 1; i < N; ++i) {
+                const int t = tok[i];
+                if (t < 0 || t >= V) flags |= GDN_DEV_TOKEN_RANGE;
+                const int p = par[i];
+                if (p < 0 || p >= i) {  // bad geometry: the node never matches
+                    flags |= GDN_DEV_TREE;
+                    par_s[i] = 0;
+                    dep_s[i] = 1;
+                    ok_s[i] = 0;
+                    continue;
+                }
+                par_s[i] = p;
+                dep_s[i] = dep_s[p] + 1;
+                ok_s[i] = ok_s[p] && t == am_s[p];
+                if (ok_s[i] && (dep_s[i] > dep_s[best_node] ||
+                                (dep_s[i] == dep_s[best_node] && path_less(par_s, i, best_node))))
+                    best_node = i;
+            }
+            accept_len[b] = dep_s[best_node];
+        }
+        accept_node[b] = best_node;
+        if (flags && dev_status) atomicOr(dev_status, flags);
+        counters[b] = 0u;  // leave the workspace zero-filled for the next call
+    }
+}
+
+int choose_splits(int rows, int V) {
+    const int sms = gdnhost::sm_count();
+    const int target = 4 * (sms > 0 ? sms : 152);
+    int s = (target + rows - 1) / rows;
+    const int by_size = (V + 2047) / 2048;  // at least ~2K logits per CTA
+    if (s > by_size) s = by_size;
+    if (s > kMaxSplits) s = kMaxSplits;
+    if (s < 1) s = 1;
+    return s;
+}
+
+}  // namespace
+
+extern "C" size_t spec_accept_workspace_bytes(int32_t batch, int32_t n_nodes) {
+    if (batch < 1 || n_nodes < 1 || n_nodes > kMaxNodes || (int64_t)batch * n_nodes > (1 << 20)) return 0;
+    return kCounterBytes(batch) + (size_t)batch * n_nodes * kMaxSplits * sizeof(unsigned long long);
+}
+
+extern "C" int spec_accept_greedy(int32_t batch, int32_t n_nodes, int32_t vocab, const float *logits,
+                                  const int32_t *tokens, const int32_t *parent_dev, int32_t *argmax_out,
+                                  int32_t *accept_len, int32_t *accept_node, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, gdn_stream_t stream) {
+    if (batch < 1 || batch > 65535 || n_nodes < 1 || n_nodes > kMaxNodes || vocab < 1 ||
+        (int64_t)batch * n_nodes > (1 << 20))
+        return GDN_ERR_DIMS;
+    if (!logits || !tokens || !argmax_out || !accept_len || !accept_node) return GDN_ERR_NULL;
+    using gdnhost::aligned_to;
+    if (!aligned_to(logits, 16) || !aligned_to(tokens, 4) || !aligned_to(argmax_out, 4) ||
+        !aligned_to(accept_len, 4) || !aligned_to(accept_node, 4) ||
+        (parent_dev && !aligned_to(parent_dev, 4)) || (dev_status && !aligned_to(dev_status, 4)))
+        return GDN_ERR_ALIGN;
+    const size_t need = spec_accept_workspace_bytes(batch, n_nodes);
+    if (!workspace || workspace_bytes < need || !aligned_to(workspace, 256)) return GDN_ERR_WORKSPACE;
+
+    const int splits = choose_splits(batch * n_nodes, vocab);
+    int chunk = (vocab + splits - 1) / splits;
+    chunk = (chunk + 3) & ~3;
+    unsigned *counters = static_cast<unsigned *>(workspace);
+    unsigned long long *keys =
+        reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + kCounterBytes(batch));
+    dim3 grid(splits, n_nodes, batch);
+    spec_accept_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        n_nodes, vocab, splits, chunk, logits, tokens, parent_dev, argmax_out, accept_len, accept_node,
+        counters, keys, dev_status);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

@@ -1,0 +1,157 @@
+"""One speculative step on the device: verify -> greedy accept -> restore.
+
+`SpecStep` owns the device buffers of a workload (all in HBM, allocated once
+through PyTorch) and queues the three C-ABI calls on one stream with no host
+synchronisation in between: the accepted node travels from
+spec_accept_greedy to gdn_rollback_restore in device memory.
+`run_host_step` is the end-to-end form of the same step: inputs come from
+pinned host memory and the accepted length / node / bonus token go back to
+the host.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import gdnspec as G
+from .workloads import GDN_BF16, Workload
+
+
+def _dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device)
+
+
+class SpecStep:
+    """Device-resident buffers and launches for one workload."""
+
+    def __init__(self, wl: Workload, device="cuda", q_scale: float = 1.0):
+        s = wl.shape
+        self.wl = wl
+        self.shape = s
+        self.device = torch.device(device)
+        self.tree = wl.parent is not None
+        self.dims = G.make_dims(s.batch, s.layers, s.h_k, s.h_v, s.d_k, s.d_v, s.conv_k,
+                                s.dtype, q_scale=q_scale)
+        self.n_nodes = s.n_nodes
+        self.n_tok = s.n_tok
+        in_dt = torch.bfloat16 if s.dtype == GDN_BF16 else torch.float32
+        dev = self.device
+        self.x = _dev(wl.x, dev, in_dt if s.dtype == GDN_BF16 else None)
+        self.a = _dev(wl.a, dev, in_dt if s.dtype == GDN_BF16 else None)
+        self.b = _dev(wl.b, dev, in_dt if s.dtype == GDN_BF16 else None)
+        self.conv_w = _dev(wl.conv_w, dev, in_dt if s.dtype == GDN_BF16 else None)
+        self.ssm_state = _dev(wl.ssm0, dev)
+        self.conv_state = _dev(wl.conv0, dev)
+        B, Y, T = s.batch, s.layers, s.n_tok
+        self.ssm_ckpt = torch.empty((B, Y, T, s.h_v, s.d_v, s.d_k), dtype=torch.float32, device=dev)
+        self.conv_ckpt = torch.empty((B, Y, T, s.conv_ch, s.conv_k - 1), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, Y, T, s.h_v, s.d_v), dtype=torch.float32, device=dev)
+        self.logits = _dev(wl.logits, dev)
+        self.tokens = _dev(wl.tokens, dev)
+        self.parent_host = wl.parent
+        self.parent = _dev(wl.parent, dev) if self.tree else None
+        self.argmax = torch.zeros((B, s.n_nodes), dtype=torch.int32, device=dev)
+        self.accept_len = torch.zeros((B,), dtype=torch.int32, device=dev)
+        self.accept_node = torch.zeros((B,), dtype=torch.int32, device=dev)
+        self.ws_bytes = G.spec_accept_workspace_bytes(B, s.n_nodes)
+        self.workspace = torch.zeros((self.ws_bytes,), dtype=torch.uint8, device=dev)
+        self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    # -- the three calls -------------------------------------------------
+    def verify(self, stream=None):
+        if self.tree:
+            G.gdn_tree_verify(self.dims, self.n_nodes, self.parent_host, self.parent, self.x, self.a,
+                              self.b, self.conv_w, self.ssm_state, self.conv_state, self.ssm_ckpt,
+                              self.conv_ckpt, self.out, self.dev_status, stream)
+        else:
+            G.gdn_verify_span(self.dims, self.n_tok, self.x, self.a, self.b, self.conv_w,
+                              self.ssm_state, self.conv_state, self.ssm_ckpt, self.conv_ckpt,
+                              self.out, stream)
+
+    def accept(self, stream=None):
+        s = self.shape
+        G.spec_accept_greedy(s.batch, s.n_nodes, s.vocab, self.logits, self.tokens, self.parent,
+                             self.argmax, self.accept_len, self.accept_node, self.workspace,
+                             self.ws_bytes, self.dev_status, stream)
+
+    def restore(self, stream=None):
+        G.gdn_rollback_restore(self.dims, self.n_tok, self.accept_node, self.ssm_ckpt, self.conv_ckpt,
+                               self.ssm_state, self.conv_state, self.dev_status, stream)
+
+    def step(self, stream=None):
+        self.verify(stream)
+        self.accept(stream)
+        self.restore(stream)
+
+    LAUNCHES_PER_STEP = 3
+
+    # -- algorithmic bytes -------------------------------------------------
+    def verify_bytes(self) -> int:
+        """Bytes the verify must move: S and conv state read once, every
+        checkpoint written once, inputs read once, o written once."""
+        s = self.shape
+        T, C, K = s.n_tok, s.conv_ch, s.conv_k
+        el = 2 if s.dtype == GDN_BF16 else 4
+        per = (s.h_v * s.d_v * s.d_k * 4 + C * (K - 1) * 4            # state read
+               + T * (s.h_v * s.d_v * s.d_k * 4 + C * (K - 1) * 4)    # checkpoints
+               + T * C * el + 2 * T * s.h_v * el                      # x, a, b
+               + T * s.h_v * s.d_v * 4)                               # o
+        weights = s.layers * C * K * el
+        return s.batch * s.layers * per + weights
+
+    def slot_bytes(self) -> int:
+        s = self.shape
+        return s.h_v * s.d_v * s.d_k * 4 + s.conv_ch * (s.conv_k - 1) * 4
+
+    def restore_bytes(self, accept_node: np.ndarray) -> int:
+        """Read + write of one slot per (request, layer) whose node > 0."""
+        moved = int(np.count_nonzero(np.asarray(accept_node) > 0))
+        return 2 * self.slot_bytes() * self.shape.layers * moved
+
+    def accept_bytes(self) -> int:
+        s = self.shape
+        return s.batch * s.n_nodes * (s.vocab * 4 + 4 + 4) + 8 * s.batch
+
+    def units(self) -> int:
+        """Verified tokens x layers (nodes x layers for trees) per step."""
+        s = self.shape
+        return s.batch * s.n_tok * s.layers
+
+
+def pinned_host_inputs(wl: Workload):
+    """The per-step inputs (x, a, b, logits, tokens[, parent]) in pinned host memory."""
+    s = wl.shape
+    in_dt = torch.bfloat16 if s.dtype == GDN_BF16 else None
+
+    def pin(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dt is not None:
+            t = t.view(dt)
+        return t.pin_memory()
+
+    d = dict(x=pin(wl.x, in_dt), a=pin(wl.a, in_dt), b=pin(wl.b, in_dt),
+             logits=pin(wl.logits), tokens=pin(wl.tokens))
+    if wl.parent is not None:
+        d["parent"] = pin(wl.parent)
+    return d
+
+
+def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None):
+    """End-to-end step through the public API: H2D copy of the step's inputs
+    from pinned memory, verify -> accept -> restore, D2H copy of the result
+    (accept_len, accept_node, argmax). Returns (h2d_bytes, d2h_bytes)."""
+    h2d = 0
+    for name in ("x", "a", "b", "logits", "tokens", "parent"):
+        if name in host:
+            dst = getattr(st, name)
+            dst.copy_(host[name], non_blocking=True)
+            h2d += host[name].numel() * host[name].element_size()
+    st.step(stream)
+    d2h = 0
+    for name in ("accept_len", "accept_node", "argmax"):
+        out_host[name].copy_(getattr(st, name), non_blocking=True)
+        d2h += out_host[name].numel() * out_host[name].element_size()
+    return h2d, d2h

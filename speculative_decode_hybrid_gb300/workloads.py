@@ -125,6 +125,8 @@ def random_tree(rng: np.random.Generator, n_nodes: int, max_depth: int) -> np.nd
 
 def _other_id(rng: np.random.Generator, vocab: int, avoid) -> int:
     avoid = set(int(t) for t in avoid)
+    if len(avoid) >= vocab:          # tiny vocabularies: nothing left to avoid
+        return int(rng.integers(0, vocab))
     while True:
         t = int(rng.integers(0, vocab))
         if t not in avoid:

@@ -1,0 +1,372 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the CPU oracle
+on the same seeded inputs.
+
+Bit-exact: accepted lengths and nodes, argmax indices, conv checkpoints
+(shifted copies of the inputs) and restored bytes (against the GPU's own
+checkpoint slot). Within 2e-3 normwise per (request, layer, slot, head)
+slice: SSM checkpoints, outputs, restored state against the oracle.
+"""
+import dataclasses
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (TOL, check_accept_vs_oracle, check_layer_vs_oracle, check_restore,
+                         ensure_built, run, slice_rel_err)
+from speculative_decode_hybrid_gb300 import gdnspec as G
+from speculative_decode_hybrid_gb300 import workloads as W
+from speculative_decode_hybrid_gb300.pipeline import SpecStep
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    ensure_built()
+
+
+def full_check(wl, layers=None, requests=None):
+    st = run(wl)
+    s = wl.shape
+    layers = list(range(s.layers)) if layers is None else layers
+    requests = list(range(s.batch)) if requests is None else requests
+    refs = {}
+    for r in requests:
+        res = oracle.verify_request(wl, r, layers=layers)
+        for y, ref in zip(layers, res):
+            check_layer_vs_oracle(st, wl, r, y, ref)
+            refs[(r, y)] = ref
+    kl, kn = check_accept_vs_oracle(st, wl)
+    check_restore(st, wl, kn, layers=layers, ref_layers=refs)
+    assert int(st.dev_status.item()) == 0
+    return st, kl, kn
+
+
+# ------------------------------------------------------------ the five workloads
+
+def test_workload0_tiny_chain():
+    full_check(W.make_workload(0, seed=0))
+
+
+def test_workload1_single_layer():
+    full_check(W.make_workload(1, seed=1))
+
+
+def test_workload2_full_size_all_layers():
+    """48 layers, span 16, batch 1 at full size; every layer against the oracle."""
+    wl = W.make_workload(2, seed=2)
+    st, kl, kn = full_check(wl)
+    assert 0 <= int(kl[0]) <= 16
+
+
+def test_workload3_tree_full_size_all_layers():
+    wl = W.make_workload(3, seed=3)
+    depth = oracle.tree_depths(wl.parent[0])[1]
+    assert depth.max() <= 16
+    st, kl, kn = full_check(wl)
+    assert int(kl[0]) == int(depth[int(kn[0])])
+
+
+def test_workload4_batched_full_size_sampled():
+    """16 requests x 48 layers (25 GiB of checkpoints): acceptance and restore
+    of every request; checkpoints of sampled (request, layer) pairs."""
+    wl = W.make_workload(4, seed=4)
+    st = run(wl)
+    kl, kn = check_accept_vs_oracle(st, wl)
+    pairs = [(0, 0), (3, 11), (7, 23), (12, 40), (15, 47)]
+    refs = {}
+    for r, y in pairs:
+        refs[(r, y)] = oracle.verify_request(wl, r, layers=[y])[0]
+        check_layer_vs_oracle(st, wl, r, y, refs[(r, y)])
+    # restored bytes of every request on sampled layers
+    for r in range(wl.shape.batch):
+        node = int(kn[r])
+        for y in (0, 29, 47):
+            g = st.ssm_state[r, y].cpu().numpy()
+            want = wl.ssm0[r, y] if node == 0 else st.ssm_ckpt[r, y, node - 1].cpu().numpy()
+            np.testing.assert_array_equal(g, want)
+    for (r, y), (ck, cc, _) in refs.items():
+        want = oracle.restore(ck, int(kn[r]), wl.ssm0[r, y])
+        assert slice_rel_err(st.ssm_state[r, y].cpu().numpy(), want, 128 * 128) <= TOL
+    assert int(st.dev_status.item()) == 0
+    assert len(set(int(k) for k in kl)) > 1  # independent acceptance per request
+
+
+# ------------------------------------------------------------ shapes and edges
+
+def shape(**kw):
+    base = dict(batch=1, layers=2, h_k=2, h_v=4, d_k=128, d_v=128, conv_k=4, n_nodes=6,
+                vocab=3000, dtype=W.GDN_BF16)
+    base.update(kw)
+    return W.Shape(**base)
+
+
+EDGE_SHAPES = {
+    "two_row_blocks_ragged": shape(h_k=1, h_v=3, d_v=192, n_nodes=6),
+    "min_rows_f32_one_token": shape(h_k=2, h_v=2, d_k=64, d_v=16, n_nodes=2, dtype=W.GDN_F32),
+    "max_tokens": shape(d_k=64, d_v=32, n_nodes=65),
+    "conv_k1": shape(conv_k=1, d_k=64, d_v=64),
+    "conv_k2": shape(conv_k=2),
+    "conv_k8": shape(conv_k=8, n_nodes=12),
+    "ratio1_batch3": shape(batch=3, h_k=4, h_v=4, d_v=48, layers=3),
+    "gqa4_dk64_bf16": shape(h_k=1, h_v=4, d_k=64, d_v=128),
+    "vocab_odd": shape(vocab=1001),
+    "vocab_tiny": shape(vocab=3, n_nodes=9),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE_SHAPES))
+def test_edge_shapes_chain(name):
+    full_check(W.draw(EDGE_SHAPES[name], seed=zlib.crc32(name.encode()) % 1000))
+
+
+@pytest.mark.parametrize("name", ["two_row_blocks_ragged", "max_tokens", "conv_k8", "ratio1_batch3",
+                                  "vocab_tiny"])
+def test_edge_shapes_tree(name):
+    s = dataclasses.replace(EDGE_SHAPES[name], tree=True)
+    full_check(W.draw(s, seed=7 + len(name)))
+
+
+def test_q_scale():
+    wl = W.draw(shape(), seed=11)
+    st = SpecStep(wl, q_scale=0.08838834764831845)
+    st.verify()
+    torch.cuda.synchronize()
+    for y in range(2):
+        ref = oracle.verify_request(wl, 0, layers=[y], q_scale=0.08838834764831845)[0]
+        check_layer_vs_oracle(st, wl, 0, y, ref)
+
+
+def test_star_and_deep_trees():
+    for par in (np.array([-1] + [0] * 9, dtype=np.int32), W.chain_parent(10),
+                np.array([-1, 0, 1, 1, 3, 0, 5, 6, 2, 8], dtype=np.int32)):
+        s = shape(n_nodes=10, tree=True)
+        wl = W.draw(s, seed=21)
+        wl.parent[0] = par
+        full_check(wl)
+
+
+# ------------------------------------------------------------ invariants on the GPU
+
+def test_gpu_restore_at_k_equals_replay_of_first_k():
+    """Verifying only the first k tokens gives, bit for bit, checkpoint k-1
+    of the full span (and restore copies exactly that slot)."""
+    wl = W.make_workload(1, seed=5)
+    full = run(wl, restore=False)
+    full_ck = full.ssm_ckpt.cpu()
+    full_cc = full.conv_ckpt.cpu()
+    full_out = full.out.cpu()
+    for k in (1, 2, 7, 16):
+        sub = dataclasses.replace(wl, shape=dataclasses.replace(wl.shape, n_nodes=k + 1),
+                                  x=wl.x[:, :, :k], a=wl.a[:, :, :k], b=wl.b[:, :, :k],
+                                  x_f=wl.x_f[:, :, :k], a_f=wl.a_f[:, :, :k], b_f=wl.b_f[:, :, :k],
+                                  logits=wl.logits[:, :k + 1], tokens=wl.tokens[:, :k + 1])
+        st = run(sub, restore=False)
+        assert torch.equal(st.ssm_ckpt.cpu()[:, :, k - 1], full_ck[:, :, k - 1])
+        assert torch.equal(st.conv_ckpt.cpu()[:, :, k - 1], full_cc[:, :, k - 1])
+        assert torch.equal(st.out.cpu()[:, :, :k], full_out[:, :, :k])
+
+
+def test_gpu_tree_that_is_a_chain_equals_chain():
+    wl = W.make_workload(1, seed=6)
+    chain = run(wl)
+    twl = dataclasses.replace(wl, shape=dataclasses.replace(wl.shape, tree=True),
+                              parent=W.chain_parent(wl.shape.n_nodes)[None, :].copy())
+    tree = run(twl)
+    assert torch.equal(chain.ssm_ckpt, tree.ssm_ckpt)
+    assert torch.equal(chain.conv_ckpt, tree.conv_ckpt)
+    assert torch.equal(chain.out, tree.out)
+    assert torch.equal(chain.accept_node, tree.accept_node)
+    assert torch.equal(chain.ssm_state, tree.ssm_state)
+
+
+def test_gpu_deterministic():
+    wl = W.make_workload(3, seed=8, layers=4)
+    a = run(wl)
+    b = run(wl)
+    for name in ("ssm_ckpt", "conv_ckpt", "out", "argmax", "accept_len", "accept_node", "ssm_state",
+                 "conv_state"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_gpu_writes_stay_in_bounds():
+    """Guard regions around every output keep their canary pattern."""
+    wl = W.draw(shape(h_k=1, h_v=3, d_v=192, n_nodes=7, batch=2), seed=9)
+    st = SpecStep(wl)
+    pad = 4096
+    canary = -12345.678
+
+    def guarded(t):
+        buf = torch.full((t.numel() + 2 * pad,), canary, dtype=t.dtype, device=t.device)
+        return buf, buf[pad:pad + t.numel()].view(t.shape)
+
+    gck, st.ssm_ckpt = guarded(st.ssm_ckpt)
+    gcc, st.conv_ckpt = guarded(st.conv_ckpt)
+    go, st.out = guarded(st.out)
+    gs, view = guarded(st.ssm_state)
+    view.copy_(st.ssm_state)
+    st.ssm_state = view
+    st.step()
+    torch.cuda.synchronize()
+    for buf in (gck, gcc, go, gs):
+        assert bool((buf[:pad] == canary).all()) and bool((buf[-pad:] == canary).all())
+    assert not bool((st.ssm_ckpt == canary).any())
+
+
+# ------------------------------------------------------------ acceptance edges
+
+def accept_only(logits, tokens, parent=None, dev_status=True):
+    B, N, V = logits.shape
+    dev = torch.device("cuda")
+    lg = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(dev)
+    tk = torch.from_numpy(np.ascontiguousarray(tokens, dtype=np.int32)).to(dev)
+    pr = None if parent is None else torch.from_numpy(np.ascontiguousarray(parent, dtype=np.int32)).to(dev)
+    am = torch.full((B, N), -7, dtype=torch.int32, device=dev)
+    kl = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    kn = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    wsb = G.spec_accept_workspace_bytes(B, N)
+    ws = torch.zeros((wsb,), dtype=torch.uint8, device=dev)
+    ds = torch.zeros((1,), dtype=torch.int32, device=dev)
+    G.spec_accept_greedy(B, N, V, lg, tk, pr, am, kl, kn, ws, wsb, ds if dev_status else None)
+    torch.cuda.synchronize()
+    return am.cpu().numpy(), kl.cpu().numpy(), kn.cpu().numpy(), int(ds.item()), ws
+
+
+def expect_oracle(logits, tokens, parent, am, kl, kn):
+    for r in range(logits.shape[0]):
+        o = oracle.accept_greedy(logits[r], tokens[r], None if parent is None else parent[r])
+        np.testing.assert_array_equal(am[r], o[0])
+        assert (int(kl[r]), int(kn[r])) == o[1:], r
+
+
+def test_accept_ties_signed_zero_and_split_boundaries():
+    g = np.random.default_rng(30)
+    V = 151936
+    logits = g.standard_normal((3, 5, V)).astype(np.float32)
+    # row 0: equal maxima far apart (different CTAs); row 1: all zeros with mixed signs
+    logits[0, 0, [70000, 5, 151935, 123456]] = 9.0
+    logits[0, 1] = 0.0
+    logits[0, 1, ::3] = -0.0
+    logits[0, 2, [151935, 151934]] = 10.0
+    logits[1, :, :] = -np.inf
+    logits[1, 3, 42] = -1e30
+    tokens = g.integers(0, V, (3, 5)).astype(np.int32)
+    am, kl, kn, ds, _ = accept_only(logits, tokens)
+    assert am[0, 0] == 5 and am[0, 1] == 0 and am[0, 2] == 151934 and am[1, 0] == 0 and am[1, 3] == 42
+    expect_oracle(logits, tokens, None, am, kl, kn)
+    assert ds == 0
+
+
+def test_accept_nan_flag_and_first_nan():
+    g = np.random.default_rng(31)
+    logits = g.standard_normal((1, 3, 4096)).astype(np.float32)
+    logits[0, 1, [3000, 17, 4000]] = np.nan
+    tokens = np.array([[0, 1, 2]], dtype=np.int32)
+    am, kl, kn, ds, _ = accept_only(logits, tokens)
+    assert am[0, 1] == 17
+    expect_oracle(logits, tokens, None, am, kl, kn)
+    assert ds & G.GDN_DEV_NAN_LOGIT
+
+
+def test_accept_all_match_and_token_range():
+    g = np.random.default_rng(32)
+    V, L = 151936, 16
+    logits = g.standard_normal((2, L + 1, V)).astype(np.float32)
+    am_ref = logits.argmax(axis=2)
+    tokens = np.zeros((2, L + 1), dtype=np.int32)
+    tokens[:, 1:] = am_ref[:, :-1]
+    tokens[1, 9] = V + 3            # out of range: a mismatch, flagged
+    am, kl, kn, ds, ws = accept_only(logits, tokens)
+    assert list(kl) == [L, 8] and list(kn) == [L, 8]
+    assert ds & G.GDN_DEV_TOKEN_RANGE
+    assert int(ws.count_nonzero().item()) > 0  # keys stay; counters are back to zero
+    expect_oracle(logits, tokens, None, am, kl, kn)
+
+
+@pytest.mark.parametrize("V", [1, 5, 1001, 4096, 151936])
+def test_accept_vocab_sizes_and_root_only(V):
+    g = np.random.default_rng(V)
+    for N in (1, 2, 17, 65):
+        logits = g.integers(-2, 3, (2, N, V)).astype(np.float32)   # many ties
+        am_ref = logits.argmax(axis=2)
+        tokens = g.integers(0, V, (2, N)).astype(np.int32)
+        mask = g.random((2, N)) < 0.7
+        for r in range(2):
+            for i in range(1, N):
+                if mask[r, i]:
+                    tokens[r, i] = am_ref[r, i - 1]
+        am, kl, kn, _, _ = accept_only(logits, tokens)
+        expect_oracle(logits, tokens, None, am, kl, kn)
+
+
+def test_accept_trees_with_duplicate_siblings_vs_oracle():
+    """Tiny vocabularies force duplicate sibling tokens: the deepest matching
+    node wins, then the lower index at the first divergence."""
+    g = np.random.default_rng(33)
+    for trial in range(20):
+        B, N, V = 16, int(g.integers(2, 24)), int(g.integers(1, 4))
+        logits = g.integers(0, 3, (B, N, V)).astype(np.float32)
+        tokens = g.integers(0, V, (B, N)).astype(np.int32)
+        parent = np.stack([W.random_tree(g, N, 16) for _ in range(B)])
+        am, kl, kn, ds, _ = accept_only(logits, tokens, parent)
+        expect_oracle(logits, tokens, parent, am, kl, kn)
+        assert ds == 0
+
+
+def test_accept_workspace_reuse_many_calls():
+    """The same workspace across calls of different shapes stays consistent."""
+    g = np.random.default_rng(34)
+    dev = torch.device("cuda")
+    wsb = G.spec_accept_workspace_bytes(16, 65)
+    ws = torch.zeros((wsb,), dtype=torch.uint8, device=dev)
+    for trial in range(12):
+        B, N, V = int(g.integers(1, 17)), int(g.integers(1, 66)), int(g.integers(1, 70000))
+        logits = g.standard_normal((B, N, V)).astype(np.float32)
+        tokens = g.integers(0, V, (B, N)).astype(np.int32)
+        lg = torch.from_numpy(logits).to(dev)
+        tk = torch.from_numpy(tokens).to(dev)
+        am = torch.empty((B, N), dtype=torch.int32, device=dev)
+        kl = torch.empty((B,), dtype=torch.int32, device=dev)
+        kn = torch.empty((B,), dtype=torch.int32, device=dev)
+        G.spec_accept_greedy(B, N, V, lg, tk, None, am, kl, kn, ws, wsb)
+        torch.cuda.synchronize()
+        expect_oracle(logits, tokens, None, am.cpu().numpy(), kl.cpu().numpy(), kn.cpu().numpy())
+
+
+# ------------------------------------------------------------ restore edges
+
+def test_restore_out_of_range_node_is_flagged_not_copied():
+    wl = W.draw(shape(batch=2), seed=40)
+    st = run(wl, restore=False)
+    before_s = st.ssm_state.clone()
+    before_c = st.conv_state.clone()
+    st.accept_node.copy_(torch.tensor([wl.shape.n_tok + 1, -1], dtype=torch.int32))
+    st.dev_status.zero_()
+    st.restore()
+    torch.cuda.synchronize()
+    assert torch.equal(st.ssm_state, before_s) and torch.equal(st.conv_state, before_c)
+    assert int(st.dev_status.item()) & G.GDN_DEV_NODE_RANGE
+    st.accept_node.copy_(torch.tensor([wl.shape.n_tok, 0], dtype=torch.int32))
+    st.restore()
+    torch.cuda.synchronize()
+    assert torch.equal(st.ssm_state[0], st.ssm_ckpt[0, :, -1])
+    assert torch.equal(st.conv_state[0], st.conv_ckpt[0, :, -1])
+    assert torch.equal(st.ssm_state[1], before_s[1])
+
+
+def test_tree_device_parent_mismatch_is_flagged():
+    """A device parent array that breaks parent[i] < i (host copy valid) is
+    caught by the kernel: flagged, and no out-of-bounds access."""
+    wl = W.draw(shape(n_nodes=6, tree=True), seed=41)
+    st = SpecStep(wl)
+    bad = wl.parent.copy()
+    bad[0, 3] = 50
+    st.parent.copy_(torch.from_numpy(bad))
+    st.verify()
+    torch.cuda.synchronize()
+    assert int(st.dev_status.item()) & G.GDN_DEV_TREE
