@@ -47,6 +47,8 @@ constexpr int kSlots = 4;
 constexpr int kRowsPerWarp = kRowsPerSlot * kSlots;    // 16
 constexpr int kMaxWarps = 8;
 constexpr int kRowsPerCta = kRowsPerWarp * kMaxWarps;  // 128
+constexpr int kColStride = 4 * kLanesPerRow;           // lane j owns columns 4j + kColStride*m + 0..3
+static_assert(kRowsPerWarp <= 16 && 16 % kRowsPerWarp == 0, "d_v is validated as a multiple of 16");
 
 struct VerifyArgs {
     int Y, H_k, H_v, d_v, C, K, T;
@@ -67,7 +69,7 @@ size_t verify_smem_bytes(int T, int DK, int K) {
 }
 
 template <int DK, bool BF16, bool TREE>
-__global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
+__global__ void __launch_bounds__(256, 2) gdn_verify_kernel(const VerifyArgs p) {
     constexpr int NV4 = DK / (4 * kLanesPerRow);  // float4 per lane per row
     extern __shared__ __align__(16) float smem[];
     const int T = p.T, K = p.K;
@@ -76,19 +78,37 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
     const int ratio = p.H_v / p.H_k;
     const int g = h / ratio;  // key head floor(h * H_k / H_v)
     const int row0 = rb * kRowsPerCta;
-    const int R = min(kRowsPerCta, p.d_v - row0);  // rows of this CTA, a multiple of 16
+    const int R = min(kRowsPerCta, p.d_v - row0);  // rows of this CTA, a multiple of kRowsPerWarp
     const int tid = threadIdx.x, nthreads = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+    const void *__restrict__ xin = p.x;
 
     float *q_s = smem;                   // [T][DK]
     float *k_s = q_s + (size_t)T * DK;   // [T][DK]
-    float *v_s = k_s + (size_t)T * DK;   // [T][128]
+    float *v_s = k_s + (size_t)T * DK;   // [T][kRowsPerCta]
     float *o_s = v_s + (size_t)T * kRowsPerCta;
     float *a_s = o_s + (size_t)T * kRowsPerCta;
     float *b_s = a_s + T;
     float *kq_s = b_s + T;
     int *par_s = reinterpret_cast<int *>(kq_s + T);  // [T+1]
     int *src_s = par_s + (T + 1);                    // [T][K]
+
+    // ---- the initial state of this thread's rows, loaded first so that its
+    //      latency overlaps the prologue below
+    const bool has_rows = warp * kRowsPerWarp < R;
+    const int j8 = lane & (kLanesPerRow - 1), rsub = lane / kLanesPerRow;
+    const size_t head_off = ((size_t)by * p.H_v + h) * (size_t)p.d_v * DK + (size_t)row0 * DK;
+    const float *s_in = p.ssm_in + head_off;
+    int lrow[kSlots];
+    float4 S[kSlots][NV4];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        lrow[s] = warp * kRowsPerWarp + s * kRowsPerSlot + rsub;
+#pragma unroll
+        for (int m = 0; m < NV4; ++m)
+            S[s][m] = has_rows ? ld4(s_in + (size_t)lrow[s] * DK + 4 * j8 + kColStride * m)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 
     // ---- tree geometry (re-checked on the device; never read out of bounds)
     if constexpr (TREE) {
@@ -129,7 +149,9 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
     }
     if constexpr (TREE) __syncthreads();  // src_s ready
 
-    // ---- conv1d + SiLU, one thread per channel, all nodes
+    // ---- conv1d + SiLU, one thread per channel, all nodes. The inputs of a
+    //      chunk of nodes are loaded together (one memory round trip per
+    //      chunk), then the chunk is computed.
     {
         const int nch = 2 * DK + R;
         const bool own_qk = (h % ratio == 0) && rb == 0;
@@ -160,51 +182,73 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
             }
             float *cck = p.conv_ckpt + (size_t)by * T * cc_tok + (size_t)c * (K - 1);
             if constexpr (!TREE) {
-                for (int t = 0; t < T; ++t) {
-                    const float xv = ld_in<BF16>(p.x, x_base + (size_t)t * p.C + c);
-                    float acc = 0.f;
+                constexpr int CH = 8;
+                for (int t0 = 0; t0 < T; t0 += CH) {
+                    float xr[CH];
 #pragma unroll
-                    for (int j = 0; j < GDN_MAX_CONV_K; ++j)
-                        if (j < K) acc = fmaf(wr[j], j < K - 1 ? st[j] : xv, acc);
-                    dst[(size_t)t * stride] = silu(acc);
+                    for (int u = 0; u < CH; ++u)
+                        xr[u] = t0 + u < T ? ld_in<BF16>(xin, x_base + (size_t)(t0 + u) * p.C + c) : 0.f;
 #pragma unroll
-                    for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
-                        if (j < K - 2) st[j] = st[j + 1];
-                        else if (j == K - 2) st[j] = xv;
-                    }
-                    if (own) {
+                    for (int u = 0; u < CH; ++u) {
+                        const int t = t0 + u;
+                        if (t < T) {
+                            const float xv = xr[u];
+                            float acc = 0.f;
 #pragma unroll
-                        for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
-                            if (j < K - 1) cck[(size_t)t * cc_tok + j] = st[j];
+                            for (int j = 0; j < GDN_MAX_CONV_K; ++j)
+                                if (j < K) acc = fmaf(wr[j], j < K - 1 ? st[j] : xv, acc);
+                            dst[(size_t)t * stride] = silu(acc);
+#pragma unroll
+                            for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
+                                if (j < K - 2) st[j] = st[j + 1];
+                                else if (j == K - 2) st[j] = xv;
+                            }
+                            if (own) {
+#pragma unroll
+                                for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
+                                    if (j < K - 1) cck[(size_t)t * cc_tok + j] = st[j];
+                            }
+                        }
                     }
                 }
             } else {
-                for (int t = 0; t < T; ++t) {
-                    float wv[GDN_MAX_CONV_K];
-                    float acc = 0.f;
+                constexpr int CH = 4;
+                for (int t0 = 0; t0 < T; t0 += CH) {
+                    float wv[CH][GDN_MAX_CONV_K];
 #pragma unroll
-                    for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
-                        wv[j] = 0.f;
-                        if (j < K) {
-                            const int s = src_s[t * K + j];
+                    for (int u = 0; u < CH; ++u) {
+#pragma unroll
+                        for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
                             float v = 0.f;
-                            if (s >= 1) {
-                                v = ld_in<BF16>(p.x, x_base + (size_t)(s - 1) * p.C + c);
-                            } else {
-                                const int slot = -1 - s;
+                            if (t0 + u < T && j < K) {
+                                const int s = src_s[(t0 + u) * K + j];
+                                if (s >= 1) {
+                                    v = ld_in<BF16>(xin, x_base + (size_t)(s - 1) * p.C + c);
+                                } else {
+                                    const int slot = -1 - s;
 #pragma unroll
-                                for (int q = 0; q < GDN_MAX_CONV_K - 1; ++q)
-                                    if (q == slot) v = st[q];
+                                    for (int q = 0; q < GDN_MAX_CONV_K - 1; ++q)
+                                        if (q == slot) v = st[q];
+                                }
                             }
-                            wv[j] = v;
-                            acc = fmaf(wr[j], v, acc);
+                            wv[u][j] = v;
                         }
                     }
-                    dst[(size_t)t * stride] = silu(acc);
-                    if (own) {
 #pragma unroll
-                        for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
-                            if (j < K - 1) cck[(size_t)t * cc_tok + j] = wv[j + 1];
+                    for (int u = 0; u < CH; ++u) {
+                        const int t = t0 + u;
+                        if (t < T) {
+                            float acc = 0.f;
+#pragma unroll
+                            for (int j = 0; j < GDN_MAX_CONV_K; ++j)
+                                if (j < K) acc = fmaf(wr[j], wv[u][j], acc);
+                            dst[(size_t)t * stride] = silu(acc);
+                            if (own) {
+#pragma unroll
+                                for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
+                                    if (j < K - 1) cck[(size_t)t * cc_tok + j] = wv[u][j + 1];
+                            }
+                        }
                     }
                 }
             }
@@ -249,21 +293,9 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
     __syncthreads();
 
     // ---- the recurrence: S in registers, one checkpoint slot per node
-    if (warp * kRowsPerWarp < R) {
-        const int j8 = lane & (kLanesPerRow - 1), rsub = lane / kLanesPerRow;
-        const size_t head_off = ((size_t)by * p.H_v + h) * (size_t)p.d_v * DK + (size_t)row0 * DK;
-        const float *s_in = p.ssm_in + head_off;
+    if (has_rows) {
         const size_t slot = (size_t)p.H_v * p.d_v * DK;
         float *ck0 = p.ssm_ckpt + ((size_t)by * T * p.H_v + h) * (size_t)p.d_v * DK + (size_t)row0 * DK;
-        int lrow[kSlots];
-        float4 S[kSlots][NV4];
-#pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
-            lrow[s] = warp * kRowsPerWarp + s * kRowsPerSlot + rsub;
-#pragma unroll
-            for (int m = 0; m < NV4; ++m)
-                S[s][m] = ld4(s_in + (size_t)lrow[s] * DK + 4 * j8 + 32 * m);
-        }
         for (int t = 0; t < T; ++t) {
             if constexpr (TREE) {
                 const int pp = par_s[t + 1];
@@ -273,14 +305,14 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
                     for (int s = 0; s < kSlots; ++s)
 #pragma unroll
                         for (int m = 0; m < NV4; ++m)
-                            S[s][m] = ld4(src + (size_t)lrow[s] * DK + 4 * j8 + 32 * m);
+                            S[s][m] = ld4(src + (size_t)lrow[s] * DK + 4 * j8 + kColStride * m);
                 }
             }
             float4 kk[NV4], qq[NV4];
 #pragma unroll
             for (int m = 0; m < NV4; ++m) {
-                kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + 32 * m);
-                qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + 32 * m);
+                kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+                qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
             }
             const float at = a_s[t], bt = b_s[t], kqt = kq_s[t];
             float u[kSlots], w[kSlots];
@@ -315,9 +347,7 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const VerifyArgs p) {
                     n.z = fmaf(c, kk[m].z, at * S[s][m].z);
                     n.w = fmaf(c, kk[m].w, at * S[s][m].w);
                     S[s][m] = n;
-                    float *dstp = ck + (size_t)lrow[s] * DK + 4 * j8 + 32 * m;
-                    if constexpr (TREE) st4(dstp, n);
-                    else st4_stream(dstp, n);
+                    st4(ck + (size_t)lrow[s] * DK + 4 * j8 + kColStride * m, n);
                 }
                 if (j8 == 0) o_s[(size_t)t * kRowsPerCta + lrow[s]] = fmaf(c, kqt, at * w[s]);
             }
@@ -346,7 +376,8 @@ int launch_verify(const VerifyArgs &a, int batch, cudaStream_t stream) {
         smem_set.store(smem, std::memory_order_relaxed);
     }
     const int nrb = (a.d_v + kRowsPerCta - 1) / kRowsPerCta;
-    const int threads = 2 * (a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta);
+    const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;  // d_v % kRowsPerWarp == 0
+    const int threads = rows / kRowsPerWarp * 32;
     dim3 grid(nrb, a.H_v, batch * a.Y);
     kern<<<grid, threads, smem, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

@@ -17,7 +17,10 @@ requests, "Sustained performance" and "Benchmark" sections):
   3  48 layers, DDTree of 23 nodes (root + 22), depth <= 16, logits [23, V]
   4  16 requests x 48 layers, span 16, per-request match probability
 
-Input recipe (per request, per layer, in draw order):
+Input recipe (per request, per layer, in draw order; request r of base seed
+s draws its layers from the stream [s + r, 1] and its acceptance inputs from
+[s + r, 2], so the accepted length does not depend on the layer count; model
+weights come from [s, 0x5EED]):
   * pre-conv channels x = [q | k | v]: q, k ~ N(0,1) drawn per key head and
     scaled to unit length per head and token; v ~ N(0,1)
   * b = logistic(N(0,1)), a ~ U(0.9, 0.999), one per value head and token
@@ -231,10 +234,12 @@ def draw(s: Shape, seed: int, *, planted: bool = True,
     conv_w = wrng.normal(0.0, 0.5, size=(s.layers, s.conv_ch, s.conv_k))
     X, A, Bg, S0, C0, L, TK, P, MP = [], [], [], [], [], [], [], [], []
     for r in range(s.batch):
-        rng = np.random.default_rng(seed + r)
-        pr = float(rng.uniform(0.3, 0.7)) if per_request_p else p
+        # separate streams: the acceptance draw does not depend on the layer count
+        rng = np.random.default_rng([seed + r, 1])
+        arng = np.random.default_rng([seed + r, 2])
+        pr = float(arng.uniform(0.3, 0.7)) if per_request_p else p
         x, a, b, s0, c0 = _draw_request(rng, s)
-        lg, tk, par = _draw_acceptance(rng, s, pr, planted)
+        lg, tk, par = _draw_acceptance(arng, s, pr, planted)
         X.append(x); A.append(a); Bg.append(b); S0.append(s0); C0.append(c0)
         L.append(lg); TK.append(tk); P.append(par); MP.append(pr)
     x = np.stack(X).astype(np.float32)
