@@ -166,6 +166,20 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None}
 
 
+def aggregate(local_time, local_units, ws, device):
+    """Whole-job figures over the ranks of a replica run: the slowest rank's
+    time (max) and the units of all ranks (sum). With one rank, unchanged."""
+    if ws <= 1:
+        return float(local_time), float(local_units)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_time)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def config_of(st, wl, kl):
     s = wl.shape
     from speculative_decode_hybrid_gb300.workloads import WORKLOAD_NAMES
@@ -245,12 +259,9 @@ def run_ours(args):
     acc_ms = [e[1].elapsed_time(e[2]) for e in ev]
     res_ms = [e[2].elapsed_time(e[3]) for e in ev]
     total_ms = sum(step_ms)
-    tot = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-    total_max_ms = float(tot.item())
     units = st.units()
-    value = units * K * ws / (total_max_ms / 1e3)
+    total_max_ms, units_all = aggregate(total_ms, units * K, ws, dev)
+    value = units_all / (total_max_ms / 1e3)
 
     hbm, peak_kind = peaks()
     vbytes = st.verify_bytes()
@@ -298,7 +309,6 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
     its inputs from pinned host memory, runs verify -> accept -> restore and
     reads the accepted length / node / argmax back; wall clock per step."""
     import torch
-    import torch.distributed as dist
     from speculative_decode_hybrid_gb300.pipeline import pinned_host_inputs, run_host_step
     host = pinned_host_inputs(wl)
     out_host = {"accept_len": torch.empty(st.accept_len.shape, dtype=torch.int32).pin_memory(),
@@ -316,11 +326,9 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
         t1 = time.perf_counter()
         if i >= 3:
             e2e_s.append(t1 - t0)
-    e2e_tot = torch.tensor([sum(e2e_s)], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(e2e_tot, op=dist.ReduceOp.MAX)
+    e2e_max_s, e2e_units = aggregate(sum(e2e_s), units * E, ws, dev)
     assert int(out_host["accept_len"][0]) == int(kl[0])
-    return {"value": units * E * ws / float(e2e_tot.item()), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": e2e_units / e2e_max_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s)}
 
 
