@@ -195,6 +195,36 @@ int spec_accept_greedy(int32_t batch, int32_t n_nodes, int32_t vocab,
  * sizes are out of range. */
 size_t spec_accept_workspace_bytes(int32_t batch, int32_t n_nodes);
 
+/* Size of the fixed device scratch behind spec_accept_greedy_static (1 MiB). */
+#define GDN_STATIC_SCRATCH_BYTES (1 << 20)
+
+/*
+ * spec_accept_greedy_static — spec_accept_greedy without a caller-supplied
+ * workspace, for callers that cannot allocate device memory: code that runs
+ * where cudaMalloc is unavailable or forbidden (for example inside an
+ * allocator-less runtime, a plugin host that owns all device memory, or a
+ * hot loop that must never reach the allocator). The pages have no
+ * counterpart of this call; it is a convenience of this library.
+ *
+ * Arguments, outputs and results are those of spec_accept_greedy, minus the
+ * workspace. The scratch is a fixed GDN_STATIC_SCRATCH_BYTES array in the
+ * library's device memory, present on every GPU that loads the library until
+ * the process exits. The first call on a device (with that device current)
+ * looks up the array's device address; make that first call before any
+ * stream capture. Every call zeroes the part of the array that must start at
+ * zero (a small cudaMemsetAsync on `stream`) and allocates nothing.
+ * All calls share the one array: calls that may overlap on the GPU (other
+ * streams, other host threads) race and must be serialised by the caller.
+ * Returns GDN_ERR_WORKSPACE when spec_accept_workspace_bytes(batch, n_nodes)
+ * exceeds GDN_STATIC_SCRATCH_BYTES (about 2,000 logit rows, e.g. batch 16 with
+ * n_nodes up to 65 fits), and the other codes of spec_accept_greedy.
+ */
+int spec_accept_greedy_static(int32_t batch, int32_t n_nodes, int32_t vocab,
+                              const float *logits, const int32_t *tokens,
+                              const int32_t *parent_dev,
+                              int32_t *argmax_out, int32_t *accept_len, int32_t *accept_node,
+                              int32_t *dev_status, gdn_stream_t stream);
+
 /*
  * gdn_rollback_restore — restore, on the device, the live SSM and conv state
  * of every request and layer to the checkpoint of its accepted node.

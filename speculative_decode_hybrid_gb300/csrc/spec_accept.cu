@@ -17,6 +17,8 @@
 //    accept_len / accept_node, then puts the counter back to zero.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "gdn_device.cuh"
 #include "gdn_host.h"
 #include "gdnspec.h"
@@ -200,5 +202,74 @@ extern "C" int spec_accept_greedy(int32_t batch, int32_t n_nodes, int32_t vocab,
     spec_accept_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         n_nodes, vocab, splits, chunk, logits, tokens, parent_dev, argmax_out, accept_len, accept_node,
         counters, keys, dev_status);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// spec_accept_greedy_static: the same acceptance for callers that cannot
+// allocate device memory. Its scratch (arrival counters + per-chunk keys)
+// lives in the fixed array below, which every GPU that loads this library
+// holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_accept_scratch[GDN_STATIC_SCRATCH_BYTES];
+
+// Device address of g_accept_scratch, looked up once per device. In host
+// code the symbol itself is only a host-side stand-in, never a device
+// address, so kernels must be given the looked-up pointer.
+constexpr int kMaxDevices = 64;
+std::once_flag g_scratch_once[kMaxDevices];
+void *g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+
+int static_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    std::call_once(g_scratch_once[dev], [dev] {
+        void *p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_accept_scratch);
+        g_scratch_ptr[dev] = g_scratch_err[dev] == cudaSuccess ? p : nullptr;
+    });
+    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return GDN_ERR_CUDA;
+    *out = g_scratch_ptr[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" int spec_accept_greedy_static(int32_t batch, int32_t n_nodes, int32_t vocab, const float *logits,
+                                         const int32_t *tokens, const int32_t *parent_dev,
+                                         int32_t *argmax_out, int32_t *accept_len, int32_t *accept_node,
+                                         int32_t *dev_status, gdn_stream_t stream) {
+    if (batch < 1 || batch > 65535 || n_nodes < 1 || n_nodes > kMaxNodes || vocab < 1 ||
+        (int64_t)batch * n_nodes > (1 << 20))
+        return GDN_ERR_DIMS;
+    if (!logits || !tokens || !argmax_out || !accept_len || !accept_node) return GDN_ERR_NULL;
+    using gdnhost::aligned_to;
+    if (!aligned_to(logits, 16) || !aligned_to(tokens, 4) || !aligned_to(argmax_out, 4) ||
+        !aligned_to(accept_len, 4) || !aligned_to(accept_node, 4) ||
+        (parent_dev && !aligned_to(parent_dev, 4)) || (dev_status && !aligned_to(dev_status, 4)))
+        return GDN_ERR_ALIGN;
+    const size_t need = spec_accept_workspace_bytes(batch, n_nodes);
+    if (need == 0 || need > (size_t)GDN_STATIC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    int rc = static_scratch(&scratch);
+    if (rc != GDN_OK) return rc;
+
+    // The array keeps whatever the previous call left: zero the arrival
+    // counters (the only part that must start at zero) on the same stream.
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, kCounterBytes(batch), st) != cudaSuccess) return GDN_ERR_CUDA;
+    const int splits = choose_splits(batch * n_nodes, vocab);
+    int chunk = (vocab + splits - 1) / splits;
+    chunk = (chunk + 3) & ~3;
+    unsigned *counters = static_cast<unsigned *>(scratch);
+    unsigned long long *keys =
+        reinterpret_cast<unsigned long long *>(static_cast<char *>(scratch) + kCounterBytes(batch));
+    dim3 grid(splits, n_nodes, batch);
+    spec_accept_kernel<<<grid, kThreads, 0, st>>>(n_nodes, vocab, splits, chunk, logits, tokens, parent_dev,
+                                                  argmax_out, accept_len, accept_node, counters, keys,
+                                                  dev_status);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -183,3 +183,25 @@ def gdn_tree_check(parent_host, batch: int, n_nodes: int, require_chain: bool = 
     ph = None if parent_host is None else np.ascontiguousarray(parent_host, dtype=np.int32)
     return int(load().gdn_tree_check(_ptr(ph), int(batch), int(n_nodes), int(bool(require_chain)),
                                      int(max_depth)))
+
+
+GDN_STATIC_SCRATCH_BYTES = 1 << 20
+
+
+def spec_accept_greedy_static(batch: int, n_nodes: int, vocab: int, logits, tokens, parent_dev,
+                              argmax_out, accept_len, accept_node, dev_status=None, stream=None) -> None:
+    """spec_accept_greedy without a workspace argument, for callers that
+    cannot allocate device memory: the library's fixed 1 MiB device scratch
+    is used instead. All calls share that scratch, so calls that may overlap
+    on the GPU must be serialised by the caller; make the first call on a
+    device before any stream capture (it looks up the scratch's address)."""
+    lib = load()
+    f = lib.spec_accept_greedy_static
+    if not getattr(f, "_gdn_typed", False):
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        f.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        f.restype = ctypes.c_int
+        f._gdn_typed = True
+    rc = f(int(batch), int(n_nodes), int(vocab), _ptr(logits), _ptr(tokens), _ptr(parent_dev),
+           _ptr(argmax_out), _ptr(accept_len), _ptr(accept_node), _ptr(dev_status), _stream(stream))
+    _ok(rc, "spec_accept_greedy_static")
