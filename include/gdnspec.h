@@ -87,7 +87,7 @@ typedef void *gdn_stream_t;
 #define GDN_DEV_TREE 0x8          /* a device parent array broke parent[i] in [0, i): that node
                                      was skipped (outputs for it are zero / unmatched) */
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define GDN_MAX_TOKENS 64         /* n_tok (= N - 1) per span */
 #define GDN_MAX_CONV_K 8
 
