@@ -10,9 +10,9 @@
 // Summary; the pages name the SSM and conv state, lucebox PR #533, Changes).
 //
 // Design (HBM-write bound: the checkpoints are ~83% of the bytes):
-//  * One CTA per (request*layer, value head, block of up to 128 value rows).
-//    Row i of S only needs k_t, q_t, a_t, b_t and v_t[i], so value rows are
-//    independent and S never leaves registers between tokens.
+//  * A work item is (request*layer, value head, block of up to 128 value
+//    rows). Row i of S only needs k_t, q_t, a_t, b_t and v_t[i], so value
+//    rows are independent and S never leaves registers between tokens.
 //  * 8 lanes own one 128-float row (16 floats each, as 4 float4 at columns
 //    4*j + 32*m), a warp holds 4 rows per "slot" and 4 slots (16 rows).
 //    Every checkpoint store is a coalesced st.global.v4: one warp
@@ -21,10 +21,17 @@
 //    8 lanes (3 xor-shuffles each). o_t = a (S_p.q) + c (k.q) with
 //    c = b (v - a S_p.k), which equals S_t q_t and needs no second
 //    dependent reduction; k.q is computed once per node in the prologue.
-//  * Prologue per CTA: conv + SiLU of its 256 q/k channels and its v
-//    channels for all nodes into shared memory, L2 norms, gates. The
-//    conv checkpoint (the last K-1 inputs) is a shifted copy of the inputs
-//    and is written here by the CTA that owns the channels.
+//  * Prologue per item: conv + SiLU of the head's 2*d_k q/k channels and its
+//    v channels for all nodes into shared memory, L2 norms, gates. The conv
+//    checkpoint (the last K-1 inputs) is a shifted copy of the inputs and is
+//    written by the item that owns the channels.
+//  * Persistent kernel (the default): 2 CTAs per SM walk the items
+//    round-robin. While an item streams its checkpoints, cp.async copies the
+//    next item's inputs (x tile, conv taps, conv state) into shared memory and
+//    its gates / parent array into registers, so the next prologue is pure
+//    on-chip compute; its state loads are issued first and overlap it.
+//    Items whose staging does not fit in shared memory (long f32 spans) use
+//    the one-item-per-CTA kernel, which loads its inputs directly.
 //  * Tree: nodes run in index order; when parent(i) != i-1 each thread
 //    reloads its rows of the parent's checkpoint, which it wrote itself
 //    (same thread, same addresses: program order makes it visible; the
@@ -48,6 +55,8 @@ constexpr int kRowsPerWarp = kRowsPerSlot * kSlots;    // 16
 constexpr int kMaxWarps = 8;
 constexpr int kRowsPerCta = kRowsPerWarp * kMaxWarps;  // 128
 constexpr int kColStride = 4 * kLanesPerRow;           // lane j owns columns 4j + kColStride*m + 0..3
+constexpr int kThreads = kMaxWarps * 32;
+constexpr size_t kMaxSmem = 227 * 1024;
 static_assert(kRowsPerWarp <= 16 && 16 % kRowsPerWarp == 0, "d_v is validated as a multiple of 16");
 
 struct VerifyArgs {
@@ -60,127 +69,294 @@ struct VerifyArgs {
     int32_t *dev_status;
 };
 
-__host__ __device__ constexpr size_t verify_smem_floats(int T, int DK) {
-    return (size_t)2 * T * DK + (size_t)2 * T * kRowsPerCta + 3 * (size_t)T;
+// One work item: (request*layer by, value head h, row block rb).
+struct Item {
+    int by, h, rb, y, bidx, g, row0, R;
+};
+
+__device__ __forceinline__ Item decode_item(const VerifyArgs &p, int it, int nrb) {
+    Item I;
+    I.rb = it % nrb;
+    const int r = it / nrb;
+    I.h = r % p.H_v;
+    I.by = r / p.H_v;
+    I.y = I.by % p.Y;
+    I.bidx = I.by / p.Y;
+    I.g = I.h / (p.H_v / p.H_k);  // key head floor(h * H_k / H_v)
+    I.row0 = I.rb * kRowsPerCta;
+    I.R = min(kRowsPerCta, p.d_v - I.row0);  // a multiple of kRowsPerWarp
+    return I;
 }
 
-size_t verify_smem_bytes(int T, int DK, int K) {
-    return verify_smem_floats(T, DK) * sizeof(float) + ((size_t)T + 1 + (size_t)T * K) * sizeof(int);
+// Global channel of local channel lc of an item: [q (DK) | k (DK) | v (R)].
+template <int DK>
+__device__ __forceinline__ int item_channel(const VerifyArgs &p, const Item &I, int lc) {
+    if (lc < DK) return I.g * DK + lc;
+    if (lc < 2 * DK) return p.H_k * DK + I.g * DK + (lc - DK);
+    return 2 * p.H_k * DK + I.h * p.d_v + I.row0 + (lc - 2 * DK);
 }
 
-template <int DK, bool BF16, bool TREE>
-__global__ void __launch_bounds__(256, 2) gdn_verify_kernel(const VerifyArgs p) {
-    constexpr int NV4 = DK / (4 * kLanesPerRow);  // float4 per lane per row
-    extern __shared__ __align__(16) float smem[];
-    const int T = p.T, K = p.K;
-    const int rb = blockIdx.x, h = blockIdx.y, by = blockIdx.z;
-    const int y = by % p.Y, bidx = by / p.Y;
-    const int ratio = p.H_v / p.H_k;
-    const int g = h / ratio;  // key head floor(h * H_k / H_v)
-    const int row0 = rb * kRowsPerCta;
-    const int R = min(kRowsPerCta, p.d_v - row0);  // rows of this CTA, a multiple of kRowsPerWarp
-    const int tid = threadIdx.x, nthreads = blockDim.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-    const void *__restrict__ xin = p.x;
+__host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
-    float *q_s = smem;                   // [T][DK]
-    float *k_s = q_s + (size_t)T * DK;   // [T][DK]
-    float *v_s = k_s + (size_t)T * DK;   // [T][kRowsPerCta]
-    float *o_s = v_s + (size_t)T * kRowsPerCta;
-    float *a_s = o_s + (size_t)T * kRowsPerCta;
-    float *b_s = a_s + T;
-    float *kq_s = b_s + T;
-    int *par_s = reinterpret_cast<int *>(kq_s + T);  // [T+1]
-    int *src_s = par_s + (T + 1);                    // [T][K]
+// Shared-memory carve-up (byte offsets), identical on host and device.
+struct Layout {
+    size_t q, k, v, o, a, b, kq, par, src, xst, wst, cst, total;
+};
 
-    // ---- the initial state of this thread's rows, loaded first so that its
-    //      latency overlaps the prologue below
-    const bool has_rows = warp * kRowsPerWarp < R;
-    const int j8 = lane & (kLanesPerRow - 1), rsub = lane / kLanesPerRow;
-    const size_t head_off = ((size_t)by * p.H_v + h) * (size_t)p.d_v * DK + (size_t)row0 * DK;
-    const float *s_in = p.ssm_in + head_off;
-    int lrow[kSlots];
+__host__ __device__ inline Layout make_layout(int T, int DK, int K, int esize, bool staged) {
+    Layout L;
+    size_t off = 0;
+    L.q = off; off = al16(off + (size_t)T * DK * 4);
+    L.k = off; off = al16(off + (size_t)T * DK * 4);
+    L.v = off; off = al16(off + (size_t)T * kRowsPerCta * 4);
+    L.o = off; off = al16(off + (size_t)T * kRowsPerCta * 4);
+    L.a = off; off = al16(off + (size_t)T * 4);
+    L.b = off; off = al16(off + (size_t)T * 4);
+    L.kq = off; off = al16(off + (size_t)T * 4);
+    L.par = off; off = al16(off + (size_t)(T + 1) * 4);
+    L.src = off; off = al16(off + (size_t)T * K * 4);
+    const size_t XS = 2 * (size_t)DK + kRowsPerCta;  // staged channels per item
+    L.xst = off; if (staged) off = al16(off + (size_t)T * XS * esize);
+    L.wst = off; if (staged) off = al16(off + XS * K * esize);
+    L.cst = off; if (staged) off = al16(off + XS * (K - 1) * 4);
+    L.total = off;
+    return L;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Tree: validated parents -> par_s, and the conv-window table src_s:
+// position j of node i's window holds the input of the node at path depth
+// depth(i) - (K-1-j) when that is >= 1, else conv-state slot K-2 + that
+// depth (encoded -1 - slot). pg is the request's parent array in global
+// memory; `pr` is pg[tid] already loaded by this thread (when tid <= T).
+__device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *pg, int pr, int *par_s,
+                                            int *src_s) {
+    const int T = p.T, K = p.K, tid = threadIdx.x;
+    for (int i = tid; i <= T; i += blockDim.x) {
+        int v = i == 0 ? -1 : (i == tid ? pr : pg[i]);
+        if (i > 0 && (v < 0 || v >= i)) {
+            v = i - 1;
+            if (p.dev_status) atomicOr(p.dev_status, GDN_DEV_TREE);
+        }
+        par_s[i] = v;
+    }
+    __syncthreads();
+    for (int i = tid + 1; i <= T; i += blockDim.x) {
+        int depth = 0;
+        for (int n = i; n > 0; n = par_s[n]) ++depth;
+        int node = i;
+        for (int j = K - 1; j >= 0; --j) {
+            const int pos = depth - (K - 1 - j);
+            if (pos >= 1) {
+                src_s[(i - 1) * K + j] = node;
+                node = par_s[node];
+            } else {
+                src_s[(i - 1) * K + j] = -1 - (K - 2 + pos);
+            }
+        }
+    }
+}
+
+// Per-head L2 norm of q and k, q scale, k.q; one warp per node.
+template <int DK>
+__device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s) {
+    constexpr int PER = DK / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int t = warp; t < p.T; t += nwarps) {
+        float qv[PER], kv[PER];
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            qv[e] = q_s[(size_t)t * DK + lane + 32 * e];
+            kv[e] = k_s[(size_t)t * DK + lane + 32 * e];
+            sq = fmaf(qv[e], qv[e], sq);
+            sk = fmaf(kv[e], kv[e], sk);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        }
+        const float iq = 1.0f / sqrtf(sq + 1e-6f);
+        const float ik = 1.0f / sqrtf(sk + 1e-6f);
+        float kq = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            qv[e] = qv[e] * iq * p.q_scale;
+            kv[e] = kv[e] * ik;
+            q_s[(size_t)t * DK + lane + 32 * e] = qv[e];
+            k_s[(size_t)t * DK + lane + 32 * e] = kv[e];
+            kq = fmaf(qv[e], kv[e], kq);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        if (lane == 0) kq_s[t] = kq;
+    }
+}
+
+// The register-resident state of this thread's rows (4 slots x NV4 float4).
+template <int DK>
+struct RowState {
+    static constexpr int NV4 = DK / (4 * kLanesPerRow);
     float4 S[kSlots][NV4];
+    int lrow[kSlots];
+};
+
+template <int DK>
+__device__ __forceinline__ void load_rows(RowState<DK> &rs, const float *src, bool has_rows) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int j8 = lane & (kLanesPerRow - 1), rsub = lane / kLanesPerRow;
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
-        lrow[s] = warp * kRowsPerWarp + s * kRowsPerSlot + rsub;
+        rs.lrow[s] = warp * kRowsPerWarp + s * kRowsPerSlot + rsub;
 #pragma unroll
-        for (int m = 0; m < NV4; ++m)
-            S[s][m] = has_rows ? ld4(s_in + (size_t)lrow[s] * DK + 4 * j8 + kColStride * m)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m < RowState<DK>::NV4; ++m)
+            rs.S[s][m] = has_rows ? ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+}
 
-    // ---- tree geometry (re-checked on the device; never read out of bounds)
+// The recurrence over all nodes of one item: one checkpoint slot per node.
+// s_in: the item's initial rows; ck0: slot 0 of the item's rows.
+template <int DK, bool TREE>
+__device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK> &rs, const float *s_in,
+                                          float *ck0, const float *q_s, const float *k_s,
+                                          const float *v_s, float *o_s, const float *a_s,
+                                          const float *b_s, const float *kq_s, const int *par_s) {
+    constexpr int NV4 = RowState<DK>::NV4;
+    const int lane = threadIdx.x & 31;
+    const int j8 = lane & (kLanesPerRow - 1);
+    const size_t slot = (size_t)p.H_v * p.d_v * DK;
+    for (int t = 0; t < p.T; ++t) {
+        if constexpr (TREE) {
+            const int pp = par_s[t + 1];
+            if (pp != t) {
+                const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s)
+#pragma unroll
+                    for (int m = 0; m < NV4; ++m)
+                        rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
+            }
+        }
+        float4 kk[NV4], qq[NV4];
+#pragma unroll
+        for (int m = 0; m < NV4; ++m) {
+            kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+            qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+        }
+        const float at = a_s[t], bt = b_s[t], kqt = kq_s[t];
+        float u[kSlots], w[kSlots];
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            u[s] = 0.f;
+            w[s] = 0.f;
+#pragma unroll
+            for (int m = 0; m < NV4; ++m) {
+                u[s] = dot4(rs.S[s][m], kk[m], u[s]);
+                w[s] = dot4(rs.S[s][m], qq[m], w[s]);
+            }
+        }
+#pragma unroll
+        for (int off = 1; off < kLanesPerRow; off <<= 1) {
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                u[s] += __shfl_xor_sync(0xffffffffu, u[s], off);
+                w[s] += __shfl_xor_sync(0xffffffffu, w[s], off);
+            }
+        }
+        float *ck = ck0 + (size_t)t * slot;
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            const float vv = v_s[(size_t)t * kRowsPerCta + rs.lrow[s]];
+            const float c = bt * (vv - at * u[s]);
+#pragma unroll
+            for (int m = 0; m < NV4; ++m) {
+                float4 n;
+                n.x = fmaf(c, kk[m].x, at * rs.S[s][m].x);
+                n.y = fmaf(c, kk[m].y, at * rs.S[s][m].y);
+                n.z = fmaf(c, kk[m].z, at * rs.S[s][m].z);
+                n.w = fmaf(c, kk[m].w, at * rs.S[s][m].w);
+                rs.S[s][m] = n;
+                st4(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n);
+            }
+            if (j8 == 0) o_s[(size_t)t * kRowsPerCta + rs.lrow[s]] = fmaf(c, kqt, at * w[s]);
+        }
+    }
+}
+
+// One conv output: sum_j w[j] * win[j] over the K-window, then SiLU.
+__device__ __forceinline__ float conv_out(const float (&wr)[GDN_MAX_CONV_K], const float (&win)[GDN_MAX_CONV_K],
+                                          int K) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < GDN_MAX_CONV_K; ++j)
+        if (j < K) acc = fmaf(wr[j], win[j], acc);
+    return silu(acc);
+}
+
+// ---------------------------------------------------------------------------
+// One item per CTA, inputs loaded directly from global memory.
+// ---------------------------------------------------------------------------
+template <int DK, bool BF16, bool TREE>
+__global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArgs p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Layout L = make_layout(p.T, DK, p.K, BF16 ? 2 : 4, false);
+    float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
+    float *v_s = reinterpret_cast<float *>(smem + L.v), *o_s = reinterpret_cast<float *>(smem + L.o);
+    float *a_s = reinterpret_cast<float *>(smem + L.a), *b_s = reinterpret_cast<float *>(smem + L.b);
+    float *kq_s = reinterpret_cast<float *>(smem + L.kq);
+    int *par_s = reinterpret_cast<int *>(smem + L.par), *src_s = reinterpret_cast<int *>(smem + L.src);
+    const int T = p.T, K = p.K;
+    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const Item I = decode_item(p, (blockIdx.z * p.H_v + blockIdx.y) * nrb + blockIdx.x, nrb);
+    const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
+    const void *__restrict__ xin = p.x;
+
+    // the initial state of this thread's rows, loaded first so that its
+    // latency overlaps the prologue below
+    const bool has_rows = warp * kRowsPerWarp < I.R;
+    const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
+    RowState<DK> rs;
+    load_rows<DK>(rs, p.ssm_in + head_off, has_rows);
+
     if constexpr (TREE) {
-        const int32_t *pg = p.parent + (size_t)bidx * (T + 1);
-        for (int i = tid; i <= T; i += nthreads) {
-            int v = i == 0 ? -1 : pg[i];
-            if (i > 0 && (v < 0 || v >= i)) {
-                v = i - 1;
-                if (p.dev_status) atomicOr(p.dev_status, GDN_DEV_TREE);
-            }
-            par_s[i] = v;
-        }
-        __syncthreads();
-        // Window table: position j of node i's conv window holds the input of
-        // the node at path depth depth(i) - (K-1-j) when that is >= 1, else
-        // conv-state slot K-2 + that depth (encoded -1 - slot).
-        for (int i = tid + 1; i <= T; i += nthreads) {
-            int depth = 0;
-            for (int n = i; n > 0; n = par_s[n]) ++depth;
-            int node = i;
-            for (int j = K - 1; j >= 0; --j) {
-                const int pos = depth - (K - 1 - j);
-                if (pos >= 1) {
-                    src_s[(i - 1) * K + j] = node;
-                    node = par_s[node];
-                } else {
-                    src_s[(i - 1) * K + j] = -1 - (K - 2 + pos);
-                }
-            }
-        }
+        const int32_t *pg = p.parent + (size_t)I.bidx * (T + 1);
+        const int pr = tid <= T ? (tid == 0 ? -1 : pg[tid]) : 0;
+        tree_tables(p, pg, pr, par_s, src_s);
     }
-
-    // ---- gates
     for (int t = tid; t < T; t += nthreads) {
-        const size_t gi = ((size_t)by * T + t) * p.H_v + h;
+        const size_t gi = ((size_t)I.by * T + t) * p.H_v + I.h;
         a_s[t] = ld_in<BF16>(p.a, gi);
         b_s[t] = ld_in<BF16>(p.b, gi);
     }
     if constexpr (TREE) __syncthreads();  // src_s ready
 
-    // ---- conv1d + SiLU, one thread per channel, all nodes. The inputs of a
-    //      chunk of nodes are loaded together (one memory round trip per
-    //      chunk), then the chunk is computed.
+    // conv1d + SiLU, one thread per channel; the inputs of a chunk of nodes
+    // are loaded together (one memory round trip per chunk)
     {
-        const int nch = 2 * DK + R;
-        const bool own_qk = (h % ratio == 0) && rb == 0;
-        const size_t x_base = (size_t)by * T * p.C;
+        const int nch = 2 * DK + I.R;
+        const bool own_qk = (I.h % (p.H_v / p.H_k) == 0) && I.rb == 0;
+        const size_t x_base = (size_t)I.by * T * p.C;
         const size_t cc_tok = (size_t)p.C * (K - 1);
         for (int lc = tid; lc < nch; lc += nthreads) {
-            int c, stride;
-            float *dst;
-            if (lc < DK) {
-                c = g * DK + lc;
-                dst = q_s + lc;
-                stride = DK;
-            } else if (lc < 2 * DK) {
-                c = p.H_k * DK + g * DK + (lc - DK);
-                dst = k_s + (lc - DK);
-                stride = DK;
-            } else {
-                c = 2 * p.H_k * DK + h * p.d_v + row0 + (lc - 2 * DK);
-                dst = v_s + (lc - 2 * DK);
-                stride = kRowsPerCta;
-            }
+            const int c = item_channel<DK>(p, I, lc);
+            float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
+            const int stride = lc < 2 * DK ? DK : kRowsPerCta;
             const bool own = lc >= 2 * DK || own_qk;
             float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
 #pragma unroll
             for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
-                wr[j] = j < K ? ld_in<BF16>(p.w, ((size_t)y * p.C + c) * K + j) : 0.f;
-                st[j] = j < K - 1 ? p.conv_in[((size_t)by * p.C + c) * (K - 1) + j] : 0.f;
+                wr[j] = j < K ? ld_in<BF16>(p.w, ((size_t)I.y * p.C + c) * K + j) : 0.f;
+                st[j] = j < K - 1 ? p.conv_in[((size_t)I.by * p.C + c) * (K - 1) + j] : 0.f;
             }
-            float *cck = p.conv_ckpt + (size_t)by * T * cc_tok + (size_t)c * (K - 1);
+            float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)c * (K - 1);
             if constexpr (!TREE) {
                 constexpr int CH = 8;
                 for (int t0 = 0; t0 < T; t0 += CH) {
@@ -192,16 +368,14 @@ __global__ void __launch_bounds__(256, 2) gdn_verify_kernel(const VerifyArgs p) 
                     for (int u = 0; u < CH; ++u) {
                         const int t = t0 + u;
                         if (t < T) {
-                            const float xv = xr[u];
-                            float acc = 0.f;
+                            float win[GDN_MAX_CONV_K];
 #pragma unroll
-                            for (int j = 0; j < GDN_MAX_CONV_K; ++j)
-                                if (j < K) acc = fmaf(wr[j], j < K - 1 ? st[j] : xv, acc);
-                            dst[(size_t)t * stride] = silu(acc);
+                            for (int j = 0; j < GDN_MAX_CONV_K; ++j) win[j] = j < K - 1 ? st[j] : xr[u];
+                            dst[(size_t)t * stride] = conv_out(wr, win, K);
 #pragma unroll
                             for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
                                 if (j < K - 2) st[j] = st[j + 1];
-                                else if (j == K - 2) st[j] = xv;
+                                else if (j == K - 2) st[j] = xr[u];
                             }
                             if (own) {
 #pragma unroll
@@ -238,11 +412,7 @@ __global__ void __launch_bounds__(256, 2) gdn_verify_kernel(const VerifyArgs p) 
                     for (int u = 0; u < CH; ++u) {
                         const int t = t0 + u;
                         if (t < T) {
-                            float acc = 0.f;
-#pragma unroll
-                            for (int j = 0; j < GDN_MAX_CONV_K; ++j)
-                                if (j < K) acc = fmaf(wr[j], wv[u][j], acc);
-                            dst[(size_t)t * stride] = silu(acc);
+                            dst[(size_t)t * stride] = conv_out(wr, wv[u], K);
                             if (own) {
 #pragma unroll
                                 for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
@@ -255,142 +425,274 @@ __global__ void __launch_bounds__(256, 2) gdn_verify_kernel(const VerifyArgs p) 
         }
     }
     __syncthreads();
-
-    // ---- per-head L2 norm of q and k, q scale, k.q; one warp per node
-    {
-        constexpr int PER = DK / 32;
-        for (int t = warp; t < T; t += nwarps) {
-            float qv[PER], kv[PER];
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) {
-                qv[e] = q_s[(size_t)t * DK + lane + 32 * e];
-                kv[e] = k_s[(size_t)t * DK + lane + 32 * e];
-                sq = fmaf(qv[e], qv[e], sq);
-                sk = fmaf(kv[e], kv[e], sk);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                sk += __shfl_xor_sync(0xffffffffu, sk, off);
-            }
-            const float iq = 1.0f / sqrtf(sq + 1e-6f);
-            const float ik = 1.0f / sqrtf(sk + 1e-6f);
-            float kq = 0.f;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) {
-                qv[e] = qv[e] * iq * p.q_scale;
-                kv[e] = kv[e] * ik;
-                q_s[(size_t)t * DK + lane + 32 * e] = qv[e];
-                k_s[(size_t)t * DK + lane + 32 * e] = kv[e];
-                kq = fmaf(qv[e], kv[e], kq);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-            if (lane == 0) kq_s[t] = kq;
-        }
-    }
+    norm_qk<DK>(p, q_s, k_s, kq_s);
     __syncthreads();
-
-    // ---- the recurrence: S in registers, one checkpoint slot per node
     if (has_rows) {
-        const size_t slot = (size_t)p.H_v * p.d_v * DK;
-        float *ck0 = p.ssm_ckpt + ((size_t)by * T * p.H_v + h) * (size_t)p.d_v * DK + (size_t)row0 * DK;
-        for (int t = 0; t < T; ++t) {
-            if constexpr (TREE) {
-                const int pp = par_s[t + 1];
-                if (pp != t) {
-                    const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
-#pragma unroll
-                    for (int s = 0; s < kSlots; ++s)
-#pragma unroll
-                        for (int m = 0; m < NV4; ++m)
-                            S[s][m] = ld4(src + (size_t)lrow[s] * DK + 4 * j8 + kColStride * m);
-                }
-            }
-            float4 kk[NV4], qq[NV4];
-#pragma unroll
-            for (int m = 0; m < NV4; ++m) {
-                kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + kColStride * m);
-                qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
-            }
-            const float at = a_s[t], bt = b_s[t], kqt = kq_s[t];
-            float u[kSlots], w[kSlots];
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) {
-                u[s] = 0.f;
-                w[s] = 0.f;
-#pragma unroll
-                for (int m = 0; m < NV4; ++m) {
-                    u[s] = dot4(S[s][m], kk[m], u[s]);
-                    w[s] = dot4(S[s][m], qq[m], w[s]);
-                }
-            }
-#pragma unroll
-            for (int off = 1; off < kLanesPerRow; off <<= 1) {
-#pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    u[s] += __shfl_xor_sync(0xffffffffu, u[s], off);
-                    w[s] += __shfl_xor_sync(0xffffffffu, w[s], off);
-                }
-            }
-            float *ck = ck0 + (size_t)t * slot;
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) {
-                const float vv = v_s[(size_t)t * kRowsPerCta + lrow[s]];
-                const float c = bt * (vv - at * u[s]);
-#pragma unroll
-                for (int m = 0; m < NV4; ++m) {
-                    float4 n;
-                    n.x = fmaf(c, kk[m].x, at * S[s][m].x);
-                    n.y = fmaf(c, kk[m].y, at * S[s][m].y);
-                    n.z = fmaf(c, kk[m].z, at * S[s][m].z);
-                    n.w = fmaf(c, kk[m].w, at * S[s][m].w);
-                    S[s][m] = n;
-                    st4(ck + (size_t)lrow[s] * DK + 4 * j8 + kColStride * m, n);
-                }
-                if (j8 == 0) o_s[(size_t)t * kRowsPerCta + lrow[s]] = fmaf(c, kqt, at * w[s]);
-            }
-        }
+        float *ck0 = p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
+        recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
     }
     __syncthreads();
-
-    // ---- o, coalesced: out[b][y][t][h][row]
-    for (int i = tid; i < T * R; i += nthreads) {
-        const int t = i / R, r = i - t * R;
-        p.out[(((size_t)by * T + t) * p.H_v + h) * p.d_v + row0 + r] = o_s[(size_t)t * kRowsPerCta + r];
+    for (int i = tid; i < T * I.R; i += nthreads) {
+        const int t = i / I.R, r = i - t * I.R;
+        p.out[(((size_t)I.by * T + t) * p.H_v + I.h) * p.d_v + I.row0 + r] = o_s[(size_t)t * kRowsPerCta + r];
     }
 }
 
-template <int DK, bool BF16, bool TREE>
-int launch_verify(const VerifyArgs &a, int batch, cudaStream_t stream) {
-    auto kern = gdn_verify_kernel<DK, BF16, TREE>;
-    const size_t smem = verify_smem_bytes(a.T, DK, a.K);
-    // Largest dynamic shared memory opted into so far, per instantiation (and
-    // per process: the attribute is set on every device the first time a
-    // larger size is needed there; raising it again is harmless).
-    static std::atomic<size_t> smem_set{48 * 1024};
-    if (smem > smem_set.load(std::memory_order_relaxed)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        smem_set.store(smem, std::memory_order_relaxed);
+// ---------------------------------------------------------------------------
+// Persistent kernel: CTAs walk the items round-robin and prefetch the next
+// item's inputs while the current one streams its checkpoints.
+// ---------------------------------------------------------------------------
+
+// Queue the asynchronous copies of item I's x tile, conv taps and conv state
+// into the staging buffers (16-byte cp.async; every source and destination
+// offset is a multiple of 16 bytes, see the host-side eligibility check).
+template <int DK, bool BF16>
+__device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I, unsigned char *xst,
+                                              unsigned char *wst, unsigned char *cst) {
+    constexpr int ES = BF16 ? 2 : 4;
+    constexpr int XS = 2 * DK + kRowsPerCta;
+    const int T = p.T, K = p.K, tid = threadIdx.x, nthreads = blockDim.x;
+    const unsigned char *xg = static_cast<const unsigned char *>(p.x);
+    const unsigned char *wg = static_cast<const unsigned char *>(p.w);
+    const unsigned char *cg = reinterpret_cast<const unsigned char *>(p.conv_in);
+    const size_t c_q = (size_t)I.g * DK, c_k = (size_t)p.H_k * DK + (size_t)I.g * DK;
+    const size_t c_v = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;
+    // x: per node, the three channel ranges [q | k | v]
+    {
+        const int cq = DK * ES / 16, cv = I.R * ES / 16, per_node = 2 * cq + cv;
+        for (int i = tid; i < T * per_node; i += nthreads) {
+            const int t = i / per_node, r = i - t * per_node;
+            size_t c0;
+            int dch, off;
+            if (r < cq) { c0 = c_q; dch = 0; off = r; }
+            else if (r < 2 * cq) { c0 = c_k; dch = DK; off = r - cq; }
+            else { c0 = c_v; dch = 2 * DK; off = r - 2 * cq; }
+            cp_async16(xst + ((size_t)t * XS + dch) * ES + (size_t)off * 16,
+                       xg + (((size_t)I.by * T + t) * p.C + c0) * ES + (size_t)off * 16);
+        }
     }
+    // conv taps [c][K] and conv state [c][K-1] of the three ranges
+    {
+        const int wq = DK * K * ES / 16, wv = I.R * K * ES / 16, wn = 2 * wq + wv;
+        for (int i = tid; i < wn; i += nthreads) {
+            size_t c0;
+            int dch, off;
+            if (i < wq) { c0 = c_q; dch = 0; off = i; }
+            else if (i < 2 * wq) { c0 = c_k; dch = DK; off = i - wq; }
+            else { c0 = c_v; dch = 2 * DK; off = i - 2 * wq; }
+            cp_async16(wst + (size_t)dch * K * ES + (size_t)off * 16,
+                       wg + ((size_t)I.y * p.C + c0) * K * ES + (size_t)off * 16);
+        }
+        const int sq = DK * (K - 1) * 4 / 16, sv = I.R * (K - 1) * 4 / 16, sn = 2 * sq + sv;
+        for (int i = tid; i < sn; i += nthreads) {
+            size_t c0;
+            int dch, off;
+            if (i < sq) { c0 = c_q; dch = 0; off = i; }
+            else if (i < 2 * sq) { c0 = c_k; dch = DK; off = i - sq; }
+            else { c0 = c_v; dch = 2 * DK; off = i - 2 * sq; }
+            cp_async16(cst + (size_t)dch * (K - 1) * 4 + (size_t)off * 16,
+                       cg + ((size_t)I.by * p.C + c0) * (K - 1) * 4 + (size_t)off * 16);
+        }
+    }
+    cp_async_commit();
+}
+
+// The small per-item values that are not contiguous: gates (thread t < T)
+// and, for trees, the parent array (thread i <= T); loaded into registers.
+template <bool BF16, bool TREE>
+__device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item &I, float &ga, float &gb,
+                                                 int &pr) {
+    const int T = p.T, tid = threadIdx.x;
+    if (tid < T) {
+        const size_t gi = ((size_t)I.by * T + tid) * p.H_v + I.h;
+        ga = ld_in<BF16>(p.a, gi);
+        gb = ld_in<BF16>(p.b, gi);
+    }
+    if constexpr (TREE) pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I.bidx * (T + 1) + tid]) : 0;
+}
+
+template <int DK, bool BF16, bool TREE>
+__global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const VerifyArgs p, int n_items) {
+    constexpr int ES = BF16 ? 2 : 4;
+    constexpr int XS = 2 * DK + kRowsPerCta;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Layout L = make_layout(p.T, DK, p.K, ES, true);
+    float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
+    float *v_s = reinterpret_cast<float *>(smem + L.v), *o_s = reinterpret_cast<float *>(smem + L.o);
+    float *a_s = reinterpret_cast<float *>(smem + L.a), *b_s = reinterpret_cast<float *>(smem + L.b);
+    float *kq_s = reinterpret_cast<float *>(smem + L.kq);
+    int *par_s = reinterpret_cast<int *>(smem + L.par), *src_s = reinterpret_cast<int *>(smem + L.src);
+    unsigned char *xst = smem + L.xst, *wst = smem + L.wst, *cst = smem + L.cst;
+    const int T = p.T, K = p.K;
+    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
+    const size_t cc_tok = (size_t)p.C * (K - 1);
+
+    int it = blockIdx.x;
+    if (it >= n_items) return;
+    float ga = 0.f, gb = 0.f;
+    int pr = 0;
+    {
+        const Item I0 = decode_item(p, it, nrb);
+        prefetch_item<DK, BF16>(p, I0, xst, wst, cst);
+        prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr);
+    }
+    while (true) {
+        const Item I = decode_item(p, it, nrb);
+        const bool has_rows = warp * kRowsPerWarp < I.R;
+        const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
+        RowState<DK> rs;
+        load_rows<DK>(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
+
+        cp_async_wait_all();
+        if (tid < T) {
+            a_s[tid] = ga;
+            b_s[tid] = gb;
+        }
+        __syncthreads();  // staged inputs and gates visible to every thread
+        if constexpr (TREE) {
+            tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s);
+            __syncthreads();
+        }
+
+        // conv1d + SiLU from the staged inputs, one thread per channel
+        {
+            const int nch = 2 * DK + I.R;
+            const bool own_qk = (I.h % (p.H_v / p.H_k) == 0) && I.rb == 0;
+            for (int lc = tid; lc < nch; lc += nthreads) {
+                const int c = item_channel<DK>(p, I, lc);
+                float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
+                const int stride = lc < 2 * DK ? DK : kRowsPerCta;
+                const bool own = lc >= 2 * DK || own_qk;
+                float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
+#pragma unroll
+                for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
+                    wr[j] = j < K ? ld_in<BF16>(wst, (size_t)lc * K + j) : 0.f;
+                    st[j] = j < K - 1 ? reinterpret_cast<const float *>(cst)[(size_t)lc * (K - 1) + j] : 0.f;
+                }
+                float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)c * (K - 1);
+                for (int t = 0; t < T; ++t) {
+                    float win[GDN_MAX_CONV_K];
+                    if constexpr (!TREE) {
+                        const float xv = ld_in<BF16>(xst, (size_t)t * XS + lc);
+#pragma unroll
+                        for (int j = 0; j < GDN_MAX_CONV_K; ++j) win[j] = j < K - 1 ? st[j] : xv;
+                        dst[(size_t)t * stride] = conv_out(wr, win, K);
+#pragma unroll
+                        for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
+                            if (j < K - 2) st[j] = st[j + 1];
+                            else if (j == K - 2) st[j] = xv;
+                        }
+                        if (own) {
+#pragma unroll
+                            for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
+                                if (j < K - 1) cck[(size_t)t * cc_tok + j] = st[j];
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
+                            float v = 0.f;
+                            if (j < K) {
+                                const int s = src_s[t * K + j];
+                                if (s >= 1) {
+                                    v = ld_in<BF16>(xst, (size_t)(s - 1) * XS + lc);
+                                } else {
+                                    const int slot = -1 - s;
+#pragma unroll
+                                    for (int q = 0; q < GDN_MAX_CONV_K - 1; ++q)
+                                        if (q == slot) v = st[q];
+                                }
+                            }
+                            win[j] = v;
+                        }
+                        dst[(size_t)t * stride] = conv_out(wr, win, K);
+                        if (own) {
+#pragma unroll
+                            for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
+                                if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j + 1];
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();  // staging consumed; q, k, v ready
+
+        const int next = it + gridDim.x;
+        if (next < n_items) {
+            const Item In = decode_item(p, next, nrb);
+            prefetch_item<DK, BF16>(p, In, xst, wst, cst);
+            prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr);
+        }
+        norm_qk<DK>(p, q_s, k_s, kq_s);
+        __syncthreads();
+        if (has_rows) {
+            float *ck0 =
+                p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
+            recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+        }
+        __syncthreads();
+        for (int i = tid; i < T * I.R; i += nthreads) {
+            const int t = i / I.R, r = i - t * I.R;
+            p.out[(((size_t)I.by * T + t) * p.H_v + I.h) * p.d_v + I.row0 + r] = o_s[(size_t)t * kRowsPerCta + r];
+        }
+        if (next >= n_items) break;
+        it = next;
+    }
+}
+
+// Raise a kernel's dynamic shared-memory limit once per size (per process;
+// raising it again is harmless).
+template <typename K>
+bool ensure_smem(K kern, size_t smem, std::atomic<size_t> &set) {
+    if (smem <= set.load(std::memory_order_relaxed)) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return false;
+    set.store(smem, std::memory_order_relaxed);
+    return true;
+}
+
+template <int DK, bool BF16, bool TREE>
+int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStream_t stream) {
     const int nrb = (a.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int n_items = batch * a.Y * a.H_v * nrb;
     const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;  // d_v % kRowsPerWarp == 0
     const int threads = rows / kRowsPerWarp * 32;
-    dim3 grid(nrb, a.H_v, batch * a.Y);
-    kern<<<grid, threads, smem, stream>>>(a);
+    const Layout Lp = make_layout(a.T, DK, a.K, BF16 ? 2 : 4, true);
+    // the persistent kernel keeps one gate / parent value per thread in registers
+    if (aligned_inputs && Lp.total <= kMaxSmem && threads > a.T) {
+        auto kern = gdn_verify_persistent<DK, BF16, TREE>;
+        static std::atomic<size_t> set{48 * 1024};
+        if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, Lp.total) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        const int sms = gdnhost::sm_count();
+        int grid = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+        if (grid > n_items) grid = n_items;
+        kern<<<grid, threads, Lp.total, stream>>>(a, n_items);
+    } else {
+        auto kern = gdn_verify_kernel<DK, BF16, TREE>;
+        static std::atomic<size_t> set{48 * 1024};
+        const Layout L = make_layout(a.T, DK, a.K, BF16 ? 2 : 4, false);
+        if (!ensure_smem(kern, L.total, set)) return GDN_ERR_CUDA;
+        dim3 grid(nrb, a.H_v, batch * a.Y);
+        kern<<<grid, threads, L.total, stream>>>(a);
+    }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 template <bool TREE>
 int dispatch_verify(const gdn_dims *d, const VerifyArgs &a, cudaStream_t stream) {
     const bool bf = d->in_dtype == GDN_BF16;
+    // cp.async staging needs 16-byte aligned x and conv taps (the offsets it
+    // copies from are then multiples of 16 bytes: C, d_k and every row block
+    // are multiples of 16 channels)
+    const bool al = gdnhost::aligned16(a.x) && gdnhost::aligned16(a.w);
     if (d->d_k == 128)
-        return bf ? launch_verify<128, true, TREE>(a, d->batch, stream)
-                  : launch_verify<128, false, TREE>(a, d->batch, stream);
-    return bf ? launch_verify<64, true, TREE>(a, d->batch, stream)
-              : launch_verify<64, false, TREE>(a, d->batch, stream);
+        return bf ? launch_verify<128, true, TREE>(a, d->batch, al, stream)
+                  : launch_verify<128, false, TREE>(a, d->batch, al, stream);
+    return bf ? launch_verify<64, true, TREE>(a, d->batch, al, stream)
+              : launch_verify<64, false, TREE>(a, d->batch, al, stream);
 }
 
 int check_common(const gdn_dims *d, int32_t n_tok, const void *x, const void *a, const void *b,

@@ -370,3 +370,32 @@ def test_tree_device_parent_mismatch_is_flagged():
     st.verify()
     torch.cuda.synchronize()
     assert int(st.dev_status.item()) & G.GDN_DEV_TREE
+
+
+# ------------------------------------------------------------ both verify kernels
+
+def test_fallback_kernel_long_f32_span():
+    """A 64-token f32 span at d_k = 128 does not fit the persistent kernel's
+    staging; the one-item-per-CTA kernel runs it."""
+    s = shape(h_k=1, h_v=2, d_k=128, d_v=128, n_nodes=65, dtype=W.GDN_F32, layers=2)
+    full_check(W.draw(s, seed=50))
+    full_check(W.draw(dataclasses.replace(s, tree=True), seed=51))
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_persistent_and_fallback_kernels_agree_bitwise(tree):
+    """An x tensor that is not 16-byte aligned cannot be staged with cp.async
+    and takes the fallback kernel; both kernels must give the same bytes."""
+    s = shape(h_k=2, h_v=6, d_v=128, n_nodes=9, layers=3, batch=2, tree=tree)
+    wl = W.draw(s, seed=52)
+    a = run(wl)
+    b = SpecStep(wl)
+    shifted = torch.empty(b.x.numel() + 8, dtype=b.x.dtype, device=b.x.device)
+    view = shifted[1:1 + b.x.numel()].view(b.x.shape)   # 2-byte offset
+    view.copy_(b.x)
+    b.x = view
+    assert b.x.data_ptr() % 16 != 0
+    b.step()
+    torch.cuda.synchronize()
+    for name in ("ssm_ckpt", "conv_ckpt", "out", "ssm_state", "conv_state", "accept_node"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
