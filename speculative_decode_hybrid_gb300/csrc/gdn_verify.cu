@@ -98,12 +98,13 @@ __device__ __forceinline__ int item_channel(const VerifyArgs &p, const Item &I, 
 
 __host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
-// Shared-memory carve-up (byte offsets), identical on host and device.
+// Shared-memory carve-up of the one-item-per-CTA kernel (byte offsets),
+// identical on host and device.
 struct Layout {
-    size_t q, k, v, o, a, b, kq, par, src, xst, wst, cst, total;
+    size_t q, k, v, o, a, b, kq, par, src, total;
 };
 
-__host__ __device__ inline Layout make_layout(int T, int DK, int K, int esize, bool staged) {
+__host__ __device__ inline Layout make_layout(int T, int DK, int K) {
     Layout L;
     size_t off = 0;
     L.q = off; off = al16(off + (size_t)T * DK * 4);
@@ -115,10 +116,6 @@ __host__ __device__ inline Layout make_layout(int T, int DK, int K, int esize, b
     L.kq = off; off = al16(off + (size_t)T * 4);
     L.par = off; off = al16(off + (size_t)(T + 1) * 4);
     L.src = off; off = al16(off + (size_t)T * K * 4);
-    const size_t XS = 2 * (size_t)DK + kRowsPerCta;  // staged channels per item
-    L.xst = off; if (staged) off = al16(off + (size_t)T * XS * esize);
-    L.wst = off; if (staged) off = al16(off + XS * K * esize);
-    L.cst = off; if (staged) off = al16(off + XS * (K - 1) * 4);
     L.total = off;
     return L;
 }
@@ -222,72 +219,91 @@ __device__ __forceinline__ void load_rows(RowState<DK> &rs, const float *src, bo
     }
 }
 
-// The recurrence over all nodes of one item: one checkpoint slot per node.
+// One node t of the recurrence for this thread's rows: one checkpoint slot.
 // s_in: the item's initial rows; ck0: slot 0 of the item's rows.
+template <int DK, bool TREE>
+__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK> &rs, int t, const float *s_in,
+                                               float *ck0, const float *q_s, const float *k_s,
+                                               const float *v_s, float *o_s, const float *a_s,
+                                               const float *b_s, const float *kq_s, const int *par_s) {
+    constexpr int NV4 = RowState<DK>::NV4;
+    const int lane = threadIdx.x & 31;
+    const int j8 = lane & (kLanesPerRow - 1);
+    const size_t slot = (size_t)p.H_v * p.d_v * DK;
+    if constexpr (TREE) {
+        const int pp = par_s[t + 1];
+        if (pp != t) {
+            const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s)
+#pragma unroll
+                for (int m = 0; m < NV4; ++m)
+                    rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
+        }
+    }
+    float4 kk[NV4], qq[NV4];
+#pragma unroll
+    for (int m = 0; m < NV4; ++m) {
+        kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+        qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+    }
+    const float at = a_s[t], bt = b_s[t], kqt = kq_s[t];
+    float u[kSlots], w[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        u[s] = 0.f;
+        w[s] = 0.f;
+#pragma unroll
+        for (int m = 0; m < NV4; ++m) {
+            u[s] = dot4(rs.S[s][m], kk[m], u[s]);
+            w[s] = dot4(rs.S[s][m], qq[m], w[s]);
+        }
+    }
+#pragma unroll
+    for (int off = 1; off < kLanesPerRow; off <<= 1) {
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            u[s] += __shfl_xor_sync(0xffffffffu, u[s], off);
+            w[s] += __shfl_xor_sync(0xffffffffu, w[s], off);
+        }
+    }
+    float *ck = ck0 + (size_t)t * slot;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        const float vv = v_s[(size_t)t * kRowsPerCta + rs.lrow[s]];
+        const float c = bt * (vv - at * u[s]);
+#pragma unroll
+        for (int m = 0; m < NV4; ++m) {
+            float4 n;
+            n.x = fmaf(c, kk[m].x, at * rs.S[s][m].x);
+            n.y = fmaf(c, kk[m].y, at * rs.S[s][m].y);
+            n.z = fmaf(c, kk[m].z, at * rs.S[s][m].z);
+            n.w = fmaf(c, kk[m].w, at * rs.S[s][m].w);
+            rs.S[s][m] = n;
+            st4(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n);
+        }
+        if (j8 == 0) o_s[(size_t)t * kRowsPerCta + rs.lrow[s]] = fmaf(c, kqt, at * w[s]);
+    }
+}
+
+// The recurrence over all nodes of one item.
 template <int DK, bool TREE>
 __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK> &rs, const float *s_in,
                                           float *ck0, const float *q_s, const float *k_s,
                                           const float *v_s, float *o_s, const float *a_s,
                                           const float *b_s, const float *kq_s, const int *par_s) {
-    constexpr int NV4 = RowState<DK>::NV4;
-    const int lane = threadIdx.x & 31;
-    const int j8 = lane & (kLanesPerRow - 1);
-    const size_t slot = (size_t)p.H_v * p.d_v * DK;
-    for (int t = 0; t < p.T; ++t) {
-        if constexpr (TREE) {
-            const int pp = par_s[t + 1];
-            if (pp != t) {
-                const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
-#pragma unroll
-                for (int s = 0; s < kSlots; ++s)
-#pragma unroll
-                    for (int m = 0; m < NV4; ++m)
-                        rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
-            }
-        }
-        float4 kk[NV4], qq[NV4];
-#pragma unroll
-        for (int m = 0; m < NV4; ++m) {
-            kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + kColStride * m);
-            qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
-        }
-        const float at = a_s[t], bt = b_s[t], kqt = kq_s[t];
-        float u[kSlots], w[kSlots];
-#pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
-            u[s] = 0.f;
-            w[s] = 0.f;
-#pragma unroll
-            for (int m = 0; m < NV4; ++m) {
-                u[s] = dot4(rs.S[s][m], kk[m], u[s]);
-                w[s] = dot4(rs.S[s][m], qq[m], w[s]);
-            }
-        }
-#pragma unroll
-        for (int off = 1; off < kLanesPerRow; off <<= 1) {
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) {
-                u[s] += __shfl_xor_sync(0xffffffffu, u[s], off);
-                w[s] += __shfl_xor_sync(0xffffffffu, w[s], off);
-            }
-        }
-        float *ck = ck0 + (size_t)t * slot;
-#pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
-            const float vv = v_s[(size_t)t * kRowsPerCta + rs.lrow[s]];
-            const float c = bt * (vv - at * u[s]);
-#pragma unroll
-            for (int m = 0; m < NV4; ++m) {
-                float4 n;
-                n.x = fmaf(c, kk[m].x, at * rs.S[s][m].x);
-                n.y = fmaf(c, kk[m].y, at * rs.S[s][m].y);
-                n.z = fmaf(c, kk[m].z, at * rs.S[s][m].z);
-                n.w = fmaf(c, kk[m].w, at * rs.S[s][m].w);
-                rs.S[s][m] = n;
-                st4(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n);
-            }
-            if (j8 == 0) o_s[(size_t)t * kRowsPerCta + rs.lrow[s]] = fmaf(c, kqt, at * w[s]);
-        }
+    for (int t = 0; t < p.T; ++t)
+        recurrence_step<DK, TREE>(p, rs, t, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+}
+
+// o of one item, from shared memory [T][kRowsPerCta] to out[b][y][t][h][row]
+// with 16-byte stores (d_v, row0 and R are multiples of 16).
+__device__ __forceinline__ void write_out(const VerifyArgs &p, const Item &I, const float *o_s) {
+    const int r4 = I.R / 4;
+    for (int i = threadIdx.x; i < p.T * r4; i += blockDim.x) {
+        const int t = i / r4, r = (i - t * r4) * 4;
+        st4(p.out + (((size_t)I.by * p.T + t) * p.H_v + I.h) * p.d_v + I.row0 + r,
+            ld4(o_s + (size_t)t * kRowsPerCta + r));
     }
 }
 
@@ -307,7 +323,7 @@ __device__ __forceinline__ float conv_out(const float (&wr)[GDN_MAX_CONV_K], con
 template <int DK, bool BF16, bool TREE>
 __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    const Layout L = make_layout(p.T, DK, p.K, BF16 ? 2 : 4, false);
+    const Layout L = make_layout(p.T, DK, p.K);
     float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
     float *v_s = reinterpret_cast<float *>(smem + L.v), *o_s = reinterpret_cast<float *>(smem + L.o);
     float *a_s = reinterpret_cast<float *>(smem + L.a), *b_s = reinterpret_cast<float *>(smem + L.b);
@@ -432,10 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
         recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
     }
     __syncthreads();
-    for (int i = tid; i < T * I.R; i += nthreads) {
-        const int t = i / I.R, r = i - t * I.R;
-        p.out[(((size_t)I.by * T + t) * p.H_v + I.h) * p.d_v + I.row0 + r] = o_s[(size_t)t * kRowsPerCta + r];
-    }
+    write_out(p, I, o_s);
 }
 
 // ---------------------------------------------------------------------------
@@ -511,19 +524,53 @@ __device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item
     if constexpr (TREE) pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I.bidx * (T + 1) + tid]) : 0;
 }
 
-template <int DK, bool BF16, bool TREE>
+// Shared-memory carve-up of the persistent kernel: the item's buffers plus
+// the staging of the next item's inputs.
+struct PipeLayout {
+    size_t q, k, v, o, a, b, kq, par, src, xst, wst, cst, total;
+};
+
+__host__ __device__ inline PipeLayout make_pipe_layout(int T, int DK, int K, int esize) {
+    PipeLayout L;
+    size_t off = 0;
+    const size_t XS = 2 * (size_t)DK + kRowsPerCta;  // staged channels per item
+    L.q = off; off = al16(off + (size_t)T * DK * 4);
+    L.k = off; off = al16(off + (size_t)T * DK * 4);
+    L.v = off; off = al16(off + (size_t)T * kRowsPerCta * 4);
+    L.o = off; off = al16(off + (size_t)T * kRowsPerCta * 4);
+    L.a = off; off = al16(off + (size_t)T * 4);
+    L.b = off; off = al16(off + (size_t)T * 4);
+    L.kq = off; off = al16(off + (size_t)T * 4);
+    L.par = off; off = al16(off + (size_t)(T + 1) * 4);
+    L.src = off; off = al16(off + (size_t)T * K * 4);
+    L.xst = off; off = al16(off + (size_t)T * XS * esize);
+    L.wst = off; off = al16(off + XS * K * esize);
+    L.cst = off; off = al16(off + XS * (K - 1) * 4);
+    L.total = off;
+    return L;
+}
+
+// Persistent kernel: CTAs walk the items round-robin; while an item streams
+// its checkpoints, the next item's inputs are copied into the staging
+// buffers, so its prologue is on-chip compute only.
+//
+// KT: the conv width as a compile-time constant (4 for Qwen3.5/3.6), or 0 to
+// read it from the arguments.
+template <int DK, bool BF16, bool TREE, int KT>
 __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const VerifyArgs p, int n_items) {
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int XS = 2 * DK + kRowsPerCta;
+    constexpr int KM = KT > 0 ? KT : GDN_MAX_CONV_K;  // unrolled window width
     extern __shared__ __align__(16) unsigned char smem[];
-    const Layout L = make_layout(p.T, DK, p.K, ES, true);
+    const int T = p.T, K = KT > 0 ? KT : p.K;
+    const PipeLayout L = make_pipe_layout(T, DK, K, ES);
     float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
     float *v_s = reinterpret_cast<float *>(smem + L.v), *o_s = reinterpret_cast<float *>(smem + L.o);
     float *a_s = reinterpret_cast<float *>(smem + L.a), *b_s = reinterpret_cast<float *>(smem + L.b);
     float *kq_s = reinterpret_cast<float *>(smem + L.kq);
     int *par_s = reinterpret_cast<int *>(smem + L.par), *src_s = reinterpret_cast<int *>(smem + L.src);
     unsigned char *xst = smem + L.xst, *wst = smem + L.wst, *cst = smem + L.cst;
-    const int T = p.T, K = p.K;
+    const float *cstf = reinterpret_cast<const float *>(cst);
     const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
     const size_t cc_tok = (size_t)p.C * (K - 1);
@@ -555,60 +602,74 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             __syncthreads();
         }
 
-        // conv1d + SiLU from the staged inputs, one thread per channel
+        // conv1d + SiLU from the staged inputs. Work unit = (channel, half of
+        // the nodes), consecutive threads on consecutive channels (coalesced
+        // conv-checkpoint stores, conflict-free staging reads). A chain keeps
+        // its K-window in registers (one staged load per output); a tree
+        // gathers each node's window along its root path.
         {
             const int nch = 2 * DK + I.R;
             const bool own_qk = (I.h % (p.H_v / p.H_k) == 0) && I.rb == 0;
-            for (int lc = tid; lc < nch; lc += nthreads) {
-                const int c = item_channel<DK>(p, I, lc);
+            const int nchunk = T >= 8 ? 2 : 1;
+            const int tc = (T + nchunk - 1) / nchunk;
+            for (int u = tid; u < nch * nchunk; u += nthreads) {
+                const int lc = u % nch, tb = (u / nch) * tc, te = min(T, tb + tc);
                 float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
                 const int stride = lc < 2 * DK ? DK : kRowsPerCta;
                 const bool own = lc >= 2 * DK || own_qk;
-                float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
+                float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)item_channel<DK>(p, I, lc) * (K - 1);
+                float wr[KM];
 #pragma unroll
-                for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
-                    wr[j] = j < K ? ld_in<BF16>(wst, (size_t)lc * K + j) : 0.f;
-                    st[j] = j < K - 1 ? reinterpret_cast<const float *>(cst)[(size_t)lc * (K - 1) + j] : 0.f;
-                }
-                float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)c * (K - 1);
-                for (int t = 0; t < T; ++t) {
-                    float win[GDN_MAX_CONV_K];
-                    if constexpr (!TREE) {
+                for (int j = 0; j < KM; ++j) wr[j] = j < K ? ld_in<BF16>(wst, (size_t)lc * K + j) : 0.f;
+                if constexpr (!TREE) {
+                    // win[j], j < K-1: sequence position tb-(K-1)+j (x row when >= 0,
+                    // else conv-state slot K-1+position)
+                    float win[KM];
+#pragma unroll
+                    for (int j = 0; j < KM; ++j) {
+                        win[j] = 0.f;
+                        if (j < K - 1) {
+                            const int sp = tb - (K - 1) + j;
+                            win[j] = sp >= 0 ? ld_in<BF16>(xst, (size_t)sp * XS + lc)
+                                             : cstf[(size_t)lc * (K - 1) + (K - 1 + sp)];
+                        }
+                    }
+                    for (int t = tb; t < te; ++t) {
                         const float xv = ld_in<BF16>(xst, (size_t)t * XS + lc);
+                        float acc = 0.f;
 #pragma unroll
-                        for (int j = 0; j < GDN_MAX_CONV_K; ++j) win[j] = j < K - 1 ? st[j] : xv;
-                        dst[(size_t)t * stride] = conv_out(wr, win, K);
+                        for (int j = 0; j < KM; ++j)
+                            if (j < K) acc = fmaf(wr[j], j < K - 1 ? win[j] : xv, acc);
+                        dst[(size_t)t * stride] = silu(acc);
 #pragma unroll
-                        for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
-                            if (j < K - 2) st[j] = st[j + 1];
-                            else if (j == K - 2) st[j] = xv;
+                        for (int j = 0; j < KM - 1; ++j) {
+                            if (j < K - 2) win[j] = win[j + 1];
+                            else if (j == K - 2) win[j] = xv;
                         }
                         if (own) {
 #pragma unroll
-                            for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
-                                if (j < K - 1) cck[(size_t)t * cc_tok + j] = st[j];
+                            for (int j = 0; j < KM - 1; ++j)
+                                if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j];
                         }
-                    } else {
+                    }
+                } else {
+                    for (int t = tb; t < te; ++t) {
+                        float win[KM];
+                        float acc = 0.f;
 #pragma unroll
-                        for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
-                            float v = 0.f;
+                        for (int j = 0; j < KM; ++j) {
+                            win[j] = 0.f;
                             if (j < K) {
-                                const int s = src_s[t * K + j];
-                                if (s >= 1) {
-                                    v = ld_in<BF16>(xst, (size_t)(s - 1) * XS + lc);
-                                } else {
-                                    const int slot = -1 - s;
-#pragma unroll
-                                    for (int q = 0; q < GDN_MAX_CONV_K - 1; ++q)
-                                        if (q == slot) v = st[q];
-                                }
+                                const int sn = src_s[t * K + j];  // >= 1: node; else -1 - conv-state slot
+                                win[j] = sn >= 1 ? ld_in<BF16>(xst, (size_t)(sn - 1) * XS + lc)
+                                                 : cstf[(size_t)lc * (K - 1) + (-1 - sn)];
+                                acc = fmaf(wr[j], win[j], acc);
                             }
-                            win[j] = v;
                         }
-                        dst[(size_t)t * stride] = conv_out(wr, win, K);
+                        dst[(size_t)t * stride] = silu(acc);
                         if (own) {
 #pragma unroll
-                            for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
+                            for (int j = 0; j < KM - 1; ++j)
                                 if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j + 1];
                         }
                     }
@@ -631,10 +692,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
         }
         __syncthreads();
-        for (int i = tid; i < T * I.R; i += nthreads) {
-            const int t = i / I.R, r = i - t * I.R;
-            p.out[(((size_t)I.by * T + t) * p.H_v + I.h) * p.d_v + I.row0 + r] = o_s[(size_t)t * kRowsPerCta + r];
-        }
+        write_out(p, I, o_s);
         if (next >= n_items) break;
         it = next;
     }
@@ -657,15 +715,25 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     const int n_items = batch * a.Y * a.H_v * nrb;
     const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;  // d_v % kRowsPerWarp == 0
     const int threads = rows / kRowsPerWarp * 32;
-    const Layout Lp = make_layout(a.T, DK, a.K, BF16 ? 2 : 4, true);
+    const PipeLayout Lp = make_pipe_layout(a.T, DK, a.K, BF16 ? 2 : 4);
     // the persistent kernel keeps one gate / parent value per thread in registers
     if (aligned_inputs && Lp.total <= kMaxSmem && threads > a.T) {
-        auto kern = gdn_verify_persistent<DK, BF16, TREE>;
-        static std::atomic<size_t> set{48 * 1024};
+        auto kern = a.K == 4 ? gdn_verify_persistent<DK, BF16, TREE, 4> : gdn_verify_persistent<DK, BF16, TREE, 0>;
+        static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
+        std::atomic<size_t> &set = a.K == 4 ? set4 : set0;
         if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, Lp.total) != cudaSuccess)
-            return GDN_ERR_CUDA;
+        // resident CTAs per SM, looked up once per (threads, shared memory)
+        // so that a step captured into a CUDA graph makes no queries
+        static std::atomic<unsigned long long> occ_key{0};
+        static std::atomic<int> occ_val{0};
+        const unsigned long long key = ((unsigned long long)Lp.total << 16) | (unsigned)threads | (a.K == 4 ? 1ull << 15 : 0);
+        int per_sm = occ_key.load(std::memory_order_acquire) == key ? occ_val.load(std::memory_order_relaxed) : 0;
+        if (per_sm == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, Lp.total) != cudaSuccess)
+                return GDN_ERR_CUDA;
+            occ_val.store(per_sm, std::memory_order_relaxed);
+            occ_key.store(key, std::memory_order_release);
+        }
         const int sms = gdnhost::sm_count();
         int grid = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
         if (grid > n_items) grid = n_items;
@@ -673,7 +741,7 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     } else {
         auto kern = gdn_verify_kernel<DK, BF16, TREE>;
         static std::atomic<size_t> set{48 * 1024};
-        const Layout L = make_layout(a.T, DK, a.K, BF16 ? 2 : 4, false);
+        const Layout L = make_layout(a.T, DK, a.K);
         if (!ensure_smem(kern, L.total, set)) return GDN_ERR_CUDA;
         dim3 grid(nrb, a.H_v, batch * a.Y);
         kern<<<grid, threads, L.total, stream>>>(a);

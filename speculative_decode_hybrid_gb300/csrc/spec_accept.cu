@@ -63,7 +63,8 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
                    unsigned *counters, unsigned long long *keys, int32_t *dev_status) {
     __shared__ unsigned long long red[kThreads / 32];
     __shared__ bool is_last;
-    __shared__ int am_s[kMaxNodes], par_s[kMaxNodes], dep_s[kMaxNodes];
+    __shared__ unsigned long long best_s[kMaxNodes];
+    __shared__ int am_s[kMaxNodes], par_s[kMaxNodes], dep_s[kMaxNodes], tok_s[kMaxNodes], pin_s[kMaxNodes];
     __shared__ unsigned char ok_s[kMaxNodes];
 
     const int split = blockIdx.x, n = blockIdx.y, b = blockIdx.z;
@@ -104,18 +105,27 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     if (!is_last) return;
     __threadfence();
 
-    // ---- last CTA of request b: finish the argmax of every row, then walk
+    // ---- last CTA of request b: finish the argmax of every row and stage the
+    //      draft tokens / parents in shared memory (one load each, in parallel),
+    //      then walk
     for (int r = tid; r < N; r += kThreads) {
-        unsigned long long k = 0ull;
-        const unsigned long long *kr = keys + ((size_t)b * N + r) * splits;
-        for (int s = 0; s < splits; ++s) k = umax64(k, __ldcg(kr + s));
-        const int am = (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
+        best_s[r] = 0ull;
+        tok_s[r] = tokens[(size_t)b * N + r];
+        pin_s[r] = parent ? parent[(size_t)b * N + r] : r - 1;
+    }
+    __syncthreads();
+    // every (row, chunk) key of the request, one independent load per thread
+    for (int i = tid; i < N * splits; i += kThreads)
+        atomicMax(&best_s[i / splits], __ldcg(keys + (size_t)b * N * splits + i));
+    __syncthreads();
+    for (int r = tid; r < N; r += kThreads) {
+        const int am = (int)(0xFFFFFFFFu - (unsigned)(best_s[r] & 0xFFFFFFFFull));
         am_s[r] = am;
         argmax_out[(size_t)b * N + r] = am;
     }
     __syncthreads();
     if (tid == 0) {
-        const int32_t *tok = tokens + (size_t)b * N;
+        const int *tok = tok_s;
         int flags = 0;
         int best_node = 0;
         if (parent == nullptr) {
@@ -128,7 +138,7 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
             }
             accept_len[b] = best_node;
         } else {
-            const int32_t *par = parent + (size_t)b * N;
+            const int *par = pin_s;
             par_s[0] = -1;
             dep_s[0] = 0;
             ok_s[0] = 1;

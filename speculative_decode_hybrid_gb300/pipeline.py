@@ -88,6 +88,27 @@ class SpecStep:
 
     LAUNCHES_PER_STEP = 3
 
+    # -- the same step as one CUDA graph ------------------------------------
+    def capture(self):
+        """Capture verify -> accept -> restore into a CUDA graph over this
+        object's fixed buffers and shapes, so that a step is one graph launch
+        (no per-kernel launch gaps). One eager step runs first, outside the
+        capture, so that every kernel attribute is already set."""
+        self.step()
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.graph(g, stream=s):
+            self.step(stream=s)
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        self._graph = g
+        return g
+
+    def replay(self):
+        """One captured step on the current stream (capture() first)."""
+        self._graph.replay()
+
     # -- algorithmic bytes -------------------------------------------------
     def verify_bytes(self) -> int:
         """Bytes the verify must move: S and conv state read once, every
@@ -139,17 +160,21 @@ def pinned_host_inputs(wl: Workload):
     return d
 
 
-def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None):
+def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None, graph: bool = False):
     """End-to-end step through the public API: H2D copy of the step's inputs
-    from pinned memory, verify -> accept -> restore, D2H copy of the result
-    (accept_len, accept_node, argmax). Returns (h2d_bytes, d2h_bytes)."""
+    from pinned memory, verify -> accept -> restore (eagerly, or as the
+    captured graph), D2H copy of the result (accept_len, accept_node,
+    argmax). Returns (h2d_bytes, d2h_bytes)."""
     h2d = 0
     for name in ("x", "a", "b", "logits", "tokens", "parent"):
         if name in host:
             dst = getattr(st, name)
             dst.copy_(host[name], non_blocking=True)
             h2d += host[name].numel() * host[name].element_size()
-    st.step(stream)
+    if graph:
+        st.replay()
+    else:
+        st.step(stream)
     d2h = 0
     for name in ("accept_len", "accept_node", "argmax"):
         out_host[name].copy_(getattr(st, name), non_blocking=True)

@@ -399,3 +399,42 @@ def test_persistent_and_fallback_kernels_agree_bitwise(tree):
     torch.cuda.synchronize()
     for name in ("ssm_ckpt", "conv_ckpt", "out", "ssm_state", "conv_state", "accept_node"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+# ------------------------------------------------------------ CUDA graph and host path
+
+@pytest.mark.parametrize("wid", [2, 3])
+def test_graph_replay_equals_eager_steps(wid):
+    """verify -> accept -> restore captured as one CUDA graph gives the same
+    bytes as the eager calls, step after step (the state evolves)."""
+    wl = W.make_workload(wid, seed=60, layers=4)
+    eager = SpecStep(wl)
+    graph = SpecStep(wl)
+    graph.capture()                    # runs one eager step first
+    eager.step()                       # keep both at the same step count
+    for _ in range(3):
+        eager.step()
+        graph.replay()
+    torch.cuda.synchronize()
+    for name in ("ssm_ckpt", "conv_ckpt", "out", "argmax", "accept_len", "accept_node", "ssm_state",
+                 "conv_state"):
+        assert torch.equal(getattr(eager, name), getattr(graph, name)), name
+
+
+def test_host_buffer_step_matches_device_step():
+    """The end-to-end path (pinned host inputs copied in, results copied back)
+    gives the device path's acceptance."""
+    from speculative_decode_hybrid_gb300.pipeline import pinned_host_inputs, run_host_step
+    wl = W.make_workload(2, seed=9, layers=2)
+    st = SpecStep(wl)
+    host = pinned_host_inputs(wl)
+    out = {"accept_len": torch.empty(1, dtype=torch.int32).pin_memory(),
+           "accept_node": torch.empty(1, dtype=torch.int32).pin_memory(),
+           "argmax": torch.empty((1, 17), dtype=torch.int32).pin_memory()}
+    h2d, d2h = run_host_step(st, host, out)
+    torch.cuda.synchronize()
+    assert h2d == wl.x.nbytes + wl.a.nbytes + wl.b.nbytes + wl.logits.nbytes + wl.tokens.nbytes
+    assert d2h == 4 + 4 + 17 * 4
+    am, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0])
+    assert int(out["accept_len"][0]) == kl == 2 and int(out["accept_node"][0]) == kn
+    np.testing.assert_array_equal(out["argmax"][0].numpy(), am)
