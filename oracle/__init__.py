@@ -63,9 +63,10 @@ def _load():
             lib.ora_argmax_f32.argtypes = [i32, vp]
             lib.ora_accept_greedy.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
             lib.ora_restore.argtypes = [lng, i32, vp, vp]
+            lib.ora_topk_f32.argtypes = [i32, vp, i32, vp, vp]
             for f in ("ora_conv1d_silu", "ora_gdn_delta_rule", "ora_gdn_delta_rule_explicit",
                       "ora_tree_depths", "ora_gdn_verify_layer", "ora_argmax_f32",
-                      "ora_accept_greedy", "ora_restore"):
+                      "ora_accept_greedy", "ora_restore", "ora_topk_f32"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -194,3 +195,13 @@ def verify_request(wl, r: int, layers=None, q_scale: float = 1.0):
                                 wl.conv_w_f[y], wl.ssm0[r, y], wl.conv0[r, y],
                                 parent=par, q_scale=q_scale))
     return res
+
+
+def topk_f32(row, k: int):
+    """Top-k of a row: NaN first, then larger values, lower index on ties.
+    Returns (idx [k] int32, val [k] float32)."""
+    row = np.ascontiguousarray(row, dtype=np.float32)
+    idx = np.zeros(k, dtype=np.int32)
+    val = np.zeros(k, dtype=np.float32)
+    _check(_load().ora_topk_f32(row.shape[0], _p(row), int(k), _p(idx), _p(val)), "topk_f32")
+    return idx, val

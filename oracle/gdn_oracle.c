@@ -335,3 +335,38 @@ int ora_restore(long long n, int node, const double *ckpt, double *state)
         memcpy(state, ckpt + (size_t)(node - 1) * (size_t)n, sizeof(double) * (size_t)n);
     return ORA_OK;
 }
+
+/* a ranks above b in the greedy order: NaN above every number (the first NaN
+ * first), otherwise the larger value, and the lower index among equals. */
+static int ranks_above(float a, int ia, float b, int ib)
+{
+    const int na = isnan(a), nb = isnan(b);
+    if (na || nb) {
+        if (na && nb) return ia < ib;
+        return na;
+    }
+    if (a > b) return 1;
+    if (a < b) return 0;
+    return ia < ib;
+}
+
+/* Top-k of one row in that order, by k rounds of selection (a draft-side
+ * top-K over the vocabulary; lucebox PR #533, Changes). idx[k], val[k]. */
+int ora_topk_f32(int V, const float *row, int k, int32_t *idx, float *val)
+{
+    if (V < 1 || k < 1 || k > V || !row || !idx || !val) return ORA_ERR_ARG;
+    unsigned char *taken = (unsigned char *)calloc((size_t)V, 1);
+    if (!taken) return ORA_ERR_NOMEM;
+    for (int r = 0; r < k; ++r) {
+        int best = -1;
+        for (int v = 0; v < V; ++v) {
+            if (taken[v]) continue;
+            if (best < 0 || ranks_above(row[v], v, row[best], best)) best = v;
+        }
+        taken[best] = 1;
+        idx[r] = best;
+        val[r] = row[best];
+    }
+    free(taken);
+    return ORA_OK;
+}

@@ -421,3 +421,27 @@ def test_oracle_tree_geometry_golden(case):
         assert rc == oracle.ORA_OK, name
     else:
         assert rc == oracle.ORA_ERR_TREE, name
+
+
+# ---------------------------------------------------------------- top-k
+
+def test_topk_matches_stable_argsort():
+    """Finite rows: the order of numpy's stable argsort of -x (larger first,
+    lower index first among equals)."""
+    g = rng(19)
+    for trial in range(40):
+        V = int(g.integers(1, 300))
+        k = int(g.integers(1, min(V, 32) + 1))
+        row = g.integers(-4, 5, V).astype(np.float32) if trial % 2 else g.standard_normal(V).astype(np.float32)
+        idx, val = oracle.topk_f32(row, k)
+        want = np.argsort(-row.astype(np.float64), kind="stable")[:k]
+        np.testing.assert_array_equal(idx, want)
+        np.testing.assert_array_equal(val, row[want])
+    assert oracle.topk_f32(np.array([3.0], dtype=np.float32), 1)[0][0] == 0
+
+
+def test_topk_nan_and_signed_zero():
+    row = np.array([0.0, np.nan, -0.0, 5.0, np.nan, -1.0], dtype=np.float32)
+    idx, _ = oracle.topk_f32(row, 6)
+    assert list(idx) == [1, 4, 3, 0, 2, 5]
+    assert oracle.topk_f32(row, 1)[0][0] == oracle.argmax_f32(row) == 1
