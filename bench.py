@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--commit", choices=["checkpoint", "replay"], default="checkpoint",
+                    help="checkpoint: per-token checkpoints + restore (the method); replay: "
+                         "verify without checkpoints, then re-run the accepted tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -190,7 +193,8 @@ def config_of(st, wl, kl):
             "state_dtype": "f32", "accepted_len": [int(k) for k in kl], "seed": wl.seed,
             "l2": "256 MiB buffer written between timed steps (outside the events); "
                   "step footprint %.2f GiB" % (st.verify_bytes() / 2 ** 30),
-            "parallelism": "replicas (independent requests per rank, no collective)"}
+            "parallelism": "replicas (independent requests per rank, no collective)",
+            "commit": getattr(st, "replay_commit", False) and "replay" or "checkpoint"}
 
 
 BENCH_WID = 2
@@ -216,6 +220,13 @@ def run_ours(args):
 
     wl = W.make_workload(BENCH_WID, seed=args.seed + 1000 * rank, layers=args.layers)
     st = SpecStep(wl, device=dev)
+    replay = args.commit == "replay"
+    if replay and st.tree:
+        raise SystemExit("the replay commit is defined for chains only")
+    st.replay_commit = replay
+    f_verify = st.verify_nockpt if replay else st.verify
+    f_commit = st.commit_replay if replay else st.restore
+    step_fn = st.step_replay if replay else st.step
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ssm0 = st.ssm_state.clone()
@@ -226,7 +237,7 @@ def run_ours(args):
             dist.barrier()
 
     for i in range(max(3, args.warmup)):
-        st.step()
+        step_fn()
     torch.cuda.synchronize(dev)
     kl = st.accept_len.cpu().numpy()
     kn = st.accept_node.cpu().numpy()
@@ -243,11 +254,11 @@ def run_ours(args):
         flush.fill_(i & 0xFF)
         e = ev[i]
         e[0].record(stream)
-        st.verify()
+        f_verify()
         e[1].record(stream)
         st.accept()
         e[2].record(stream)
-        st.restore()
+        f_commit()
         e[3].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -266,7 +277,7 @@ def run_ours(args):
     #      events around every replay, L2 flushed between replays
     graph_ok = True
     try:
-        st.capture()
+        st.capture(replay_commit=replay)
         for _ in range(3):
             st.replay()
         torch.cuda.synchronize(dev)
@@ -298,10 +309,10 @@ def run_ours(args):
     value = units_all / (total_max_ms / 1e3)
 
     hbm, peak_kind = peaks()
-    vbytes = st.verify_bytes()
+    vbytes = st.verify_bytes() if not replay else st.replay_bytes(np.zeros(st.shape.batch, dtype=int)) - st.accept_bytes()
     ver_mean_s = statistics.mean(ver_ms) / 1e3
     achieved = vbytes / ver_mean_s / 1e9
-    step_bytes = vbytes + st.accept_bytes() + st.restore_bytes(kn)
+    step_bytes = (vbytes + st.accept_bytes() + st.restore_bytes(kn)) if not replay else st.replay_bytes(kl)
     step_gbs = step_bytes / (statistics.mean(gstep_ms) / 1e3) / 1e9
 
     # ---- end to end through the public API, host buffers, copies timed
@@ -317,9 +328,10 @@ def run_ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": total_max_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(st, wl, kl),
-        "roofline": {"bound": "hbm", "kernel": "gdn_verify_kernel (gdn_verify_span)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "gdn_verify_persistent (%s)" % ("gdn_verify_span_nockpt" if replay else "gdn_verify_span"),
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": peak_kind, "traffic": recorded_traffic(),
+                     "peak_source": peak_kind, "traffic": None if replay else recorded_traffic(),
                      "algorithmic_bytes_per_launch": vbytes,
                      "verify_us_mean": ver_mean_s * 1e6,
                      "verify_us_median": statistics.median(ver_ms) * 1e3,
@@ -330,7 +342,7 @@ def run_ours(args):
         "mode": "cuda_graph" if graph_ok else "eager",
         "eager": {"value": eager_value, "ms_per_step": eager_max_ms / K},
         "clocks": clocks,
-        "gpu_launches": SpecStep.LAUNCHES_PER_STEP * K,
+        "gpu_launches": (SpecStep.LAUNCHES_PER_STEP_REPLAY if replay else SpecStep.LAUNCHES_PER_STEP) * K,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

@@ -90,6 +90,7 @@ typedef void *gdn_stream_t;
 /* Limits of this library. */
 #define GDN_MAX_TOKENS 64         /* n_tok (= N - 1) per span */
 #define GDN_MAX_CONV_K 8
+#define GDN_MAX_TOPK 32           /* k of spec_topk */
 
 /*
  * Model and batch dimensions shared by the verify and restore calls.
@@ -178,8 +179,8 @@ int gdn_tree_verify(const gdn_dims *dims, int32_t n_nodes,
  *              The bonus token is argmax_out[b][accept_node[b]].
  *   workspace  device scratch of at least spec_accept_workspace_bytes(B, N)
  *              bytes, 256-byte aligned, ZERO-FILLED before its first use; every
- *              call leaves it zero-filled again. Calls that overlap in time must
- *              not share a workspace.
+ *              call leaves every byte it used zero again, so one workspace serves
+ *              calls of any shape. Calls that overlap in time must not share it.
  *   dev_status nullable, device int32: GDN_DEV_TOKEN_RANGE / NAN_LOGIT / TREE bits.
  * Limits: 1 <= N <= GDN_MAX_TOKENS + 1, 1 <= V < 2^31, B * N <= 2^20.
  * Returns GDN_OK or GDN_ERR_{NULL,DIMS,WORKSPACE,CUDA}.
@@ -245,6 +246,60 @@ int gdn_rollback_restore(const gdn_dims *dims, int32_t n_tok,
                          const float *ssm_ckpt, const float *conv_ckpt,
                          float *ssm_state, float *conv_state,
                          int32_t *dev_status, gdn_stream_t stream);
+
+/*
+ * Replay commit (the conservative alternative to checkpoints): verify without
+ * writing any checkpoint, then, once the accepted length is known, re-run
+ * only the accepted tokens from the live state and update it in place.
+ * (openinfer PR #626, What Changed: commit restores the canonical state and
+ * replays the accepted target span; Future Work: a lower-overhead commit.)
+ * Restoring checkpoint k and replaying the first k tokens give the same
+ * bytes. Chains only: a tree's branches need the per-node states.
+ *
+ * gdn_verify_span_nockpt — gdn_verify_span writing only `out` (no ssm or
+ * conv checkpoints); the live state is read, never written.
+ */
+int gdn_verify_span_nockpt(const gdn_dims *dims, int32_t n_tok,
+                           const void *x, const void *a, const void *b, const void *conv_w,
+                           const float *ssm_in, const float *conv_in, float *out,
+                           gdn_stream_t stream);
+
+/*
+ * gdn_commit_replay — for every request b with k = accept_len_dev[b] in
+ * [1, n_tok], re-run conv + recurrence over tokens 0..k-1 of the span (the
+ * same x, a, b, conv_w as the verify call, layouts of gdn_verify_span) from
+ * ssm_state / conv_state and overwrite both with the state after token k-1.
+ * k = 0 leaves the request untouched; k outside [0, n_tok] changes nothing
+ * and sets GDN_DEV_NODE_RANGE in *dev_status (nullable). Two kernels on
+ * `stream` (the state replay, then the conv-state update).
+ * Returns GDN_OK or GDN_ERR_{NULL,DIMS,ALIGN,DTYPE,CUDA}.
+ */
+int gdn_commit_replay(const gdn_dims *dims, int32_t n_tok, const int32_t *accept_len_dev,
+                      const void *x, const void *a, const void *b, const void *conv_w,
+                      float *ssm_state, float *conv_state, int32_t *dev_status,
+                      gdn_stream_t stream);
+
+/*
+ * spec_topk — the k best logits of each row in the greedy order: larger value
+ * first, lower index among equal values, every NaN above every number (the
+ * first NaN first; flagged GDN_DEV_NAN_LOGIT), -0.0 equal to +0.0. For
+ * draft-side tree construction (lucebox PR #533, Changes: draft top-K on the
+ * GPU's logits).
+ *   logits  [rows][V] f32 (device, 16-byte aligned)
+ *   idx_out [rows][k] int32, val_out [rows][k] f32 (device): the k indices and
+ *           their logits, best first
+ *   workspace: at least spec_topk_workspace_bytes(rows, k) bytes of device
+ *           memory, 256-byte aligned, zero-filled before first use; every call
+ *           leaves it zero-filled. Overlapping calls must not share it.
+ * Limits: 1 <= k <= GDN_MAX_TOPK, k <= V, 1 <= rows <= 65535.
+ * Returns GDN_OK or GDN_ERR_{NULL,DIMS,ALIGN,WORKSPACE,CUDA}.
+ */
+int spec_topk(int32_t rows, int32_t vocab, int32_t k, const float *logits,
+              int32_t *idx_out, float *val_out, void *workspace, size_t workspace_bytes,
+              int32_t *dev_status, gdn_stream_t stream);
+
+/* Bytes of workspace spec_topk needs; 0 if the sizes are out of range. */
+size_t spec_topk_workspace_bytes(int32_t rows, int32_t k);
 
 /*
  * gdn_tree_check — host-only geometry check of B parent arrays of n_nodes

@@ -41,4 +41,28 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
 
 __device__ __forceinline__ float silu(float y) { return y / (1.0f + expf(-y)); }
 
+// Greedy-order key of logit f at index idx: the order-preserving bits of the
+// value in the high word (every NaN maps to the top, -0.0 is folded into
+// +0.0) and ~idx in the low word, so a larger key is a larger value or, among
+// equal values, a lower index. Every real key is > 0.
+__device__ __forceinline__ unsigned long long make_key(float f, unsigned idx) {
+    unsigned u = __float_as_uint(f);
+    unsigned ord;
+    if (f != f) {
+        ord = 0xFFFFFFFFu;
+    } else {
+        if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
+        ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ unsigned key_index(unsigned long long key) {
+    return 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
 }  // namespace gdndev

@@ -3,11 +3,12 @@
 // split SSM and convolution state on-device; lucebox PR #506, Summary: fast
 // rollback from F32 checkpoints, no replay).
 //
-// grid (chunks, B*Y): every CTA reads the accepted node of its request from
-// device memory (no host round trip), returns at once for node 0 (verify
-// never touched the live state) and otherwise copies its share of the
-// 16-byte vectors of slot node-1: 8 independent loads in flight per thread,
-// then 8 stores. The copy is bit-exact.
+// grid (chunks, B*Y), sized for 8 resident CTAs per SM (64 warps): every CTA
+// reads the accepted node of its request from device memory (no host round
+// trip), returns at once for node 0 (verify never touched the live state)
+// and otherwise copies its share of the 16-byte vectors of slot node-1, 4
+// independent loads in flight per thread, then 4 stores. The copy is
+// bit-exact.
 #include <cuda_runtime.h>
 
 #include "gdn_device.cuh"
@@ -17,11 +18,14 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 8;
+constexpr int kUnroll = 4;
+constexpr int kCtasPerSm = 8;
 
+// Copy n4 16-byte vectors, this thread taking begin, begin + step, ...
+// (32-bit offsets: the host routes slots of 2^31 vectors or more elsewhere).
 __device__ __forceinline__ void copy_range4(const float4 *__restrict__ src, float4 *__restrict__ dst,
-                                            size_t n4, size_t begin, size_t step) {
-    size_t i = begin;
+                                            unsigned n4, unsigned begin, unsigned step) {
+    unsigned i = begin;
     for (; i + (kUnroll - 1) * step < n4; i += kUnroll * step) {
         float4 v[kUnroll];
 #pragma unroll
@@ -32,7 +36,7 @@ __device__ __forceinline__ void copy_range4(const float4 *__restrict__ src, floa
     for (; i < n4; i += step) dst[i] = __ldcs(src + i);
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 gdn_restore_kernel(int Y, int T, size_t ssm_slot, size_t conv_slot, const int32_t *__restrict__ accept_node,
                    const float *__restrict__ ssm_ckpt, const float *__restrict__ conv_ckpt,
                    float *__restrict__ ssm_state, float *__restrict__ conv_state, int32_t *dev_status) {
@@ -45,21 +49,21 @@ gdn_restore_kernel(int Y, int T, size_t ssm_slot, size_t conv_slot, const int32_
             atomicOr(dev_status, GDN_DEV_NODE_RANGE);
         return;
     }
-    const size_t begin = (size_t)blockIdx.x * kThreads + threadIdx.x;
-    const size_t step = (size_t)gridDim.x * kThreads;
+    const unsigned begin = blockIdx.x * kThreads + threadIdx.x;
+    const unsigned step = gridDim.x * kThreads;
     {
         const float4 *src = reinterpret_cast<const float4 *>(ssm_ckpt + ((size_t)by * T + (node - 1)) * ssm_slot);
         float4 *dst = reinterpret_cast<float4 *>(ssm_state + (size_t)by * ssm_slot);
-        copy_range4(src, dst, ssm_slot / 4, begin, step);
+        copy_range4(src, dst, (unsigned)(ssm_slot / 4), begin, step);
     }
     if (conv_slot > 0) {
         const float *src = conv_ckpt + ((size_t)by * T + (node - 1)) * conv_slot;
         float *dst = conv_state + (size_t)by * conv_slot;
         if ((conv_slot & 3) == 0) {
-            copy_range4(reinterpret_cast<const float4 *>(src), reinterpret_cast<float4 *>(dst), conv_slot / 4,
-                        begin, step);
+            copy_range4(reinterpret_cast<const float4 *>(src), reinterpret_cast<float4 *>(dst),
+                        (unsigned)(conv_slot / 4), begin, step);
         } else {
-            for (size_t i = begin; i < conv_slot; i += step) dst[i] = src[i];
+            for (unsigned i = begin; i < conv_slot; i += step) dst[i] = src[i];
         }
     }
 }
@@ -82,9 +86,10 @@ extern "C" int gdn_rollback_restore(const gdn_dims *d, int32_t n_tok, const int3
 
     const size_t ssm_slot = gdnhost::ssm_slot_elems(d);
     const size_t conv_slot = gdnhost::conv_slot_elems(d);
+    if (ssm_slot >= (1ull << 31) || conv_slot >= (1ull << 31)) return GDN_ERR_DIMS;
     const int rows = d->batch * d->layers;
     const int sms = gdnhost::sm_count();
-    const int target = 4 * (sms > 0 ? sms : 152);
+    const int target = kCtasPerSm * (sms > 0 ? sms : 152);
     int chunks = (target + rows - 1) / rows;
     const size_t per_cta_min = (size_t)kThreads * kUnroll;  // float4 per CTA, at least one full round
     const size_t max_chunks = (ssm_slot / 4 + per_cta_min - 1) / per_cta_min;

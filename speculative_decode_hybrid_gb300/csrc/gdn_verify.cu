@@ -64,9 +64,10 @@ struct VerifyArgs {
     float q_scale;
     const void *x, *a, *b, *w;
     const float *ssm_in, *conv_in;
-    float *ssm_ckpt, *conv_ckpt, *out;
+    float *ssm_ckpt, *conv_ckpt, *out;  // ssm_ckpt / conv_ckpt NULL: no checkpoints
     const int32_t *parent;  // [B][T+1] for trees, nullptr for chains
     int32_t *dev_status;
+    float *ssm_out;         // replay commit: the live state, updated in place
 };
 
 // One work item: (request*layer by, value head h, row block rb).
@@ -162,10 +163,10 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
 
 // Per-head L2 norm of q and k, q scale, k.q; one warp per node.
 template <int DK>
-__device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s) {
+__device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s, int count) {
     constexpr int PER = DK / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int t = warp; t < p.T; t += nwarps) {
+    for (int t = warp; t < count; t += nwarps) {
         float qv[PER], kv[PER];
         float sq = 0.f, sk = 0.f;
 #pragma unroll
@@ -280,7 +281,7 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
             n.z = fmaf(c, kk[m].z, at * rs.S[s][m].z);
             n.w = fmaf(c, kk[m].w, at * rs.S[s][m].w);
             rs.S[s][m] = n;
-            st4(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n);
+            if (p.ssm_ckpt) st4(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n);
         }
         if (j8 == 0) o_s[(size_t)t * kRowsPerCta + rs.lrow[s]] = fmaf(c, kqt, at * w[s]);
     }
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
             const int c = item_channel<DK>(p, I, lc);
             float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
             const int stride = lc < 2 * DK ? DK : kRowsPerCta;
-            const bool own = lc >= 2 * DK || own_qk;
+            const bool own = (lc >= 2 * DK || own_qk) && p.conv_ckpt != nullptr;
             float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
 #pragma unroll
             for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
         }
     }
     __syncthreads();
-    norm_qk<DK>(p, q_s, k_s, kq_s);
+    norm_qk<DK>(p, q_s, k_s, kq_s, p.T);
     __syncthreads();
     if (has_rows) {
         float *ck0 = p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
@@ -616,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
                 const int lc = u % nch, tb = (u / nch) * tc, te = min(T, tb + tc);
                 float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
                 const int stride = lc < 2 * DK ? DK : kRowsPerCta;
-                const bool own = lc >= 2 * DK || own_qk;
+                const bool own = (lc >= 2 * DK || own_qk) && p.conv_ckpt != nullptr;
                 float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)item_channel<DK>(p, I, lc) * (K - 1);
                 float wr[KM];
 #pragma unroll
@@ -684,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             prefetch_item<DK, BF16>(p, In, xst, wst, cst);
             prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr);
         }
-        norm_qk<DK>(p, q_s, k_s, kq_s);
+        norm_qk<DK>(p, q_s, k_s, kq_s, p.T);
         __syncthreads();
         if (has_rows) {
             float *ck0 =
@@ -696,6 +697,118 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         if (next >= n_items) break;
         it = next;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Replay commit: re-run the accepted tokens of a chain from the live state.
+// ---------------------------------------------------------------------------
+
+// One item per CTA, like gdn_verify_kernel, over the first Te = accept_len[b]
+// tokens only; writes the final rows of S back into the live state. The
+// conv window comes from the (not yet updated) live conv state.
+template <int DK, bool BF16>
+__global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArgs p, const int32_t *accept_len) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Layout L = make_layout(p.T, DK, p.K);
+    float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
+    float *v_s = reinterpret_cast<float *>(smem + L.v), *o_s = reinterpret_cast<float *>(smem + L.o);
+    float *a_s = reinterpret_cast<float *>(smem + L.a), *b_s = reinterpret_cast<float *>(smem + L.b);
+    float *kq_s = reinterpret_cast<float *>(smem + L.kq);
+    const int T = p.T, K = p.K;
+    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const Item I = decode_item(p, (blockIdx.z * p.H_v + blockIdx.y) * nrb + blockIdx.x, nrb);
+    const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
+    const int Te = accept_len[I.bidx];
+    if (Te <= 0 || Te > T) {
+        if (Te != 0 && p.dev_status && tid == 0 && I.y == 0 && I.h == 0 && I.rb == 0)
+            atomicOr(p.dev_status, GDN_DEV_NODE_RANGE);
+        return;
+    }
+    const bool has_rows = warp * kRowsPerWarp < I.R;
+    const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
+    RowState<DK> rs;
+    load_rows<DK>(rs, p.ssm_out + head_off, has_rows);
+    for (int t = tid; t < Te; t += nthreads) {
+        const size_t gi = ((size_t)I.by * T + t) * p.H_v + I.h;
+        a_s[t] = ld_in<BF16>(p.a, gi);
+        b_s[t] = ld_in<BF16>(p.b, gi);
+    }
+    {
+        const int nch = 2 * DK + I.R;
+        const size_t x_base = (size_t)I.by * T * p.C;
+        for (int lc = tid; lc < nch; lc += nthreads) {
+            const int c = item_channel<DK>(p, I, lc);
+            float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
+            const int stride = lc < 2 * DK ? DK : kRowsPerCta;
+            float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
+#pragma unroll
+            for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
+                wr[j] = j < K ? ld_in<BF16>(p.w, ((size_t)I.y * p.C + c) * K + j) : 0.f;
+                st[j] = j < K - 1 ? p.conv_in[((size_t)I.by * p.C + c) * (K - 1) + j] : 0.f;
+            }
+            constexpr int CH = 8;
+            for (int t0 = 0; t0 < Te; t0 += CH) {
+                float xr[CH];
+#pragma unroll
+                for (int u = 0; u < CH; ++u)
+                    xr[u] = t0 + u < Te ? ld_in<BF16>(p.x, x_base + (size_t)(t0 + u) * p.C + c) : 0.f;
+#pragma unroll
+                for (int u = 0; u < CH; ++u) {
+                    const int t = t0 + u;
+                    if (t < Te) {
+                        float win[GDN_MAX_CONV_K];
+#pragma unroll
+                        for (int j = 0; j < GDN_MAX_CONV_K; ++j) win[j] = j < K - 1 ? st[j] : xr[u];
+                        dst[(size_t)t * stride] = conv_out(wr, win, K);
+#pragma unroll
+                        for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
+                            if (j < K - 2) st[j] = st[j + 1];
+                            else if (j == K - 2) st[j] = xr[u];
+                        }
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    norm_qk<DK>(p, q_s, k_s, kq_s, Te);
+    __syncthreads();
+    if (has_rows) {
+        const float *s_in = p.ssm_out + head_off;
+        for (int t = 0; t < Te; ++t)
+            recurrence_step<DK, false>(p, rs, t, s_in, nullptr, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, nullptr);
+        const int lane = tid & 31, j8 = lane & (kLanesPerRow - 1);
+#pragma unroll
+        for (int s2 = 0; s2 < kSlots; ++s2)
+#pragma unroll
+            for (int m = 0; m < RowState<DK>::NV4; ++m)
+                st4(p.ssm_out + head_off + (size_t)rs.lrow[s2] * DK + 4 * j8 + kColStride * m, rs.S[s2][m]);
+    }
+}
+
+// The live conv state after the replayed tokens: the last K-1 inputs of
+// [conv_state, x_0 .. x_{k-1}], one thread per channel (reads before writes).
+template <bool BF16>
+__global__ void __launch_bounds__(256) gdn_conv_state_kernel(const VerifyArgs p, const int32_t *accept_len,
+                                                            float *conv_state) {
+    const int by = blockIdx.y, bidx = by / p.Y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const int K = p.K, T = p.T;
+    const int k = accept_len[bidx];
+    if (c >= p.C || k <= 0 || k > T) return;
+    float *cs = conv_state + ((size_t)by * p.C + c) * (K - 1);
+    float nw[GDN_MAX_CONV_K];
+#pragma unroll
+    for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j) {
+        nw[j] = 0.f;
+        if (j < K - 1) {
+            const int sp = k - (K - 1) + j;  // sequence position: x row when >= 0
+            nw[j] = sp >= 0 ? ld_in<BF16>(p.x, ((size_t)by * T + sp) * p.C + c) : cs[K - 1 + sp];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
+        if (j < K - 1) cs[j] = nw[j];
 }
 
 // Raise a kernel's dynamic shared-memory limit once per size (per process;
@@ -803,6 +916,7 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
     v.out = out;
     v.parent = parent;
     v.dev_status = dev_status;
+    v.ssm_out = nullptr;
     return v;
 }
 
@@ -836,4 +950,68 @@ extern "C" int gdn_tree_verify(const gdn_dims *d, int32_t n_nodes, const int32_t
     const VerifyArgs v = make_args(d, n_nodes - 1, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt,
                                    conv_ckpt, out, parent_dev, dev_status);
     return dispatch_verify<true>(d, v, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_verify_span_nockpt(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
+                                      const void *b, const void *conv_w, const float *ssm_in,
+                                      const float *conv_in, float *out, gdn_stream_t stream) {
+    int rc = gdnhost::check_dims(d, n_tok);
+    if (rc != GDN_OK) return rc;
+    if (!x || !a || !b || !conv_w || !ssm_in || !out) return GDN_ERR_NULL;
+    if (d->conv_k > 1 && !conv_in) return GDN_ERR_NULL;
+    const size_t es = d->in_dtype == GDN_BF16 ? 2 : 4;
+    using gdnhost::aligned16;
+    using gdnhost::aligned_to;
+    if (!aligned_to(x, es) || !aligned_to(a, es) || !aligned_to(b, es) || !aligned_to(conv_w, es))
+        return GDN_ERR_ALIGN;
+    if (!aligned16(ssm_in) || !aligned16(out) || (d->conv_k > 1 && !aligned16(conv_in))) return GDN_ERR_ALIGN;
+    const VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, nullptr, nullptr, out,
+                                   nullptr, nullptr);
+    return dispatch_verify<false>(d, v, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_commit_replay(const gdn_dims *d, int32_t n_tok, const int32_t *accept_len_dev,
+                                 const void *x, const void *a, const void *b, const void *conv_w,
+                                 float *ssm_state, float *conv_state, int32_t *dev_status,
+                                 gdn_stream_t stream) {
+    int rc = gdnhost::check_dims(d, n_tok);
+    if (rc != GDN_OK) return rc;
+    if (!accept_len_dev || !x || !a || !b || !conv_w || !ssm_state) return GDN_ERR_NULL;
+    if (d->conv_k > 1 && !conv_state) return GDN_ERR_NULL;
+    const size_t es = d->in_dtype == GDN_BF16 ? 2 : 4;
+    using gdnhost::aligned16;
+    using gdnhost::aligned_to;
+    if (!aligned_to(x, es) || !aligned_to(a, es) || !aligned_to(b, es) || !aligned_to(conv_w, es) ||
+        !aligned_to(accept_len_dev, 4) || (dev_status && !aligned_to(dev_status, 4)))
+        return GDN_ERR_ALIGN;
+    if (!aligned16(ssm_state) || (d->conv_k > 1 && !aligned16(conv_state))) return GDN_ERR_ALIGN;
+    VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_state, conv_state, nullptr, nullptr, nullptr,
+                             nullptr, dev_status);
+    v.ssm_out = ssm_state;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int nrb = (d->d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int rows = d->d_v < kRowsPerCta ? d->d_v : kRowsPerCta;
+    const int threads = rows / kRowsPerWarp * 32;
+    const Layout L = make_layout(n_tok, d->d_k, d->conv_k);
+    const dim3 grid(nrb, d->h_v, d->batch * d->layers);
+    const bool bf = d->in_dtype == GDN_BF16;
+    if (d->d_k == 128) {
+        auto kern = bf ? gdn_replay_kernel<128, true> : gdn_replay_kernel<128, false>;
+        static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
+        if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
+        kern<<<grid, threads, L.total, st>>>(v, accept_len_dev);
+    } else {
+        auto kern = bf ? gdn_replay_kernel<64, true> : gdn_replay_kernel<64, false>;
+        static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
+        if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
+        kern<<<grid, threads, L.total, st>>>(v, accept_len_dev);
+    }
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    if (d->conv_k > 1) {
+        const dim3 g2((d->conv_ch + 255) / 256, d->batch * d->layers);
+        if (bf) gdn_conv_state_kernel<true><<<g2, 256, 0, st>>>(v, accept_len_dev, conv_state);
+        else gdn_conv_state_kernel<false><<<g2, 256, 0, st>>>(v, accept_len_dev, conv_state);
+        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
 }

@@ -14,7 +14,8 @@
 //    per-request arrival counter. The last CTA of a request (threadfence +
 //    atomic counter, no spinning) reduces the keys of every row of that
 //    request, writes argmax_out, walks the chain or tree once and writes
-//    accept_len / accept_node, then puts the counter back to zero.
+//    accept_len / accept_node, then puts the keys and the counter it used back
+//    to zero (so a later call of any shape finds a zero-filled workspace).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -28,23 +29,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxSplits = 64;
 constexpr int kMaxNodes = GDN_MAX_TOKENS + 1;
+static_assert(kMaxNodes <= kThreads, "one thread per node");
 constexpr size_t kCounterBytes(int32_t batch) { return (((size_t)batch * 4 + 255) / 256) * 256; }
 
-__device__ __forceinline__ unsigned long long make_key(float f, unsigned idx) {
-    unsigned u = __float_as_uint(f);
-    unsigned ord;
-    if (f != f) {
-        ord = 0xFFFFFFFFu;
-    } else {
-        if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
-        ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    }
-    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
-}
-
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
-    return a > b ? a : b;
-}
+using gdndev::make_key;
+using gdndev::umax64;
 
 // Among two distinct matching nodes of equal depth: is i's root path lower
 // than j's at the first divergence?
@@ -69,6 +58,10 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
 
     const int split = blockIdx.x, n = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
+    // the request's draft tokens / parents, loaded now so that the last CTA
+    // does not wait for them after the ticket
+    const int my_tok = tid < N ? tokens[(size_t)b * N + tid] : 0;
+    const int my_par = tid < N ? (parent ? parent[(size_t)b * N + tid] : tid - 1) : 0;
     const float *row = logits + ((size_t)b * N + n) * (size_t)V;
     const int lo = split * chunk;
     const int hi = min(V, lo + chunk);
@@ -108,15 +101,18 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     // ---- last CTA of request b: finish the argmax of every row and stage the
     //      draft tokens / parents in shared memory (one load each, in parallel),
     //      then walk
-    for (int r = tid; r < N; r += kThreads) {
-        best_s[r] = 0ull;
-        tok_s[r] = tokens[(size_t)b * N + r];
-        pin_s[r] = parent ? parent[(size_t)b * N + r] : r - 1;
+    if (tid < N) {  // N <= kMaxNodes <= kThreads
+        best_s[tid] = 0ull;
+        tok_s[tid] = my_tok;
+        pin_s[tid] = my_par;
     }
     __syncthreads();
     // every (row, chunk) key of the request, one independent load per thread
-    for (int i = tid; i < N * splits; i += kThreads)
-        atomicMax(&best_s[i / splits], __ldcg(keys + (size_t)b * N * splits + i));
+    for (int i = tid; i < N * splits; i += kThreads) {
+        unsigned long long *kp = keys + (size_t)b * N * splits + i;
+        atomicMax(&best_s[i / splits], __ldcg(kp));
+        *kp = 0ull;  // leave the workspace zero-filled
+    }
     __syncthreads();
     for (int r = tid; r < N; r += kThreads) {
         const int am = (int)(0xFFFFFFFFu - (unsigned)(best_s[r] & 0xFFFFFFFFull));

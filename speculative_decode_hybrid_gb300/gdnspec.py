@@ -39,10 +39,12 @@ GDN_DEV_TREE = 0x8
 
 GDN_MAX_TOKENS = 64
 GDN_MAX_CONV_K = 8
+GDN_MAX_TOPK = 32
 
 EXPORTED = ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
             "spec_accept_workspace_bytes", "gdn_rollback_restore", "gdn_tree_check",
-            "gdn_status_str")
+            "gdn_status_str", "gdn_verify_span_nockpt", "gdn_commit_replay", "spec_topk",
+            "spec_topk_workspace_bytes")
 
 
 class GdnError(RuntimeError):
@@ -89,11 +91,17 @@ def load(path: Optional[str] = None):
         lib.spec_accept_workspace_bytes.argtypes = [i32, i32]
         lib.spec_accept_workspace_bytes.restype = sz
         lib.gdn_rollback_restore.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.spec_topk.argtypes = [i32, i32, i32, vp, vp, vp, vp, sz, vp, vp]
+        lib.spec_topk_workspace_bytes.argtypes = [i32, i32]
+        lib.spec_topk_workspace_bytes.restype = sz
+        lib.gdn_verify_span_nockpt.argtypes = [dp, i32] + [vp] * 7 + [vp]
+        lib.gdn_commit_replay.argtypes = [dp, i32] + [vp] * 9
         lib.gdn_tree_check.argtypes = [vp, i32, i32, i32, i32]
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
         for f in ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
-                  "gdn_rollback_restore", "gdn_tree_check"):
+                  "gdn_rollback_restore", "gdn_tree_check", "gdn_verify_span_nockpt",
+                  "gdn_commit_replay", "spec_topk"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -174,6 +182,33 @@ def gdn_rollback_restore(dims: gdn_dims, n_tok: int, accept_node_dev, ssm_ckpt, 
                                      _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(ssm_state),
                                      _ptr(conv_state), _ptr(dev_status), _stream(stream))
     _ok(rc, "gdn_rollback_restore")
+
+
+def gdn_verify_span_nockpt(dims: gdn_dims, n_tok: int, x, a, b, conv_w, ssm_in, conv_in, out,
+                           stream=None) -> None:
+    rc = load().gdn_verify_span_nockpt(ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b),
+                                       _ptr(conv_w), _ptr(ssm_in), _ptr(conv_in), _ptr(out),
+                                       _stream(stream))
+    _ok(rc, "gdn_verify_span_nockpt")
+
+
+def gdn_commit_replay(dims: gdn_dims, n_tok: int, accept_len_dev, x, a, b, conv_w, ssm_state,
+                      conv_state, dev_status=None, stream=None) -> None:
+    rc = load().gdn_commit_replay(ctypes.byref(dims), int(n_tok), _ptr(accept_len_dev), _ptr(x), _ptr(a),
+                                  _ptr(b), _ptr(conv_w), _ptr(ssm_state), _ptr(conv_state),
+                                  _ptr(dev_status), _stream(stream))
+    _ok(rc, "gdn_commit_replay")
+
+
+def spec_topk_workspace_bytes(rows: int, k: int) -> int:
+    return int(load().spec_topk_workspace_bytes(int(rows), int(k)))
+
+
+def spec_topk(rows: int, vocab: int, k: int, logits, idx_out, val_out, workspace, workspace_bytes: int,
+              dev_status=None, stream=None) -> None:
+    rc = load().spec_topk(int(rows), int(vocab), int(k), _ptr(logits), _ptr(idx_out), _ptr(val_out),
+                          _ptr(workspace), int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    _ok(rc, "spec_topk")
 
 
 def gdn_tree_check(parent_host, batch: int, n_nodes: int, require_chain: bool = False,

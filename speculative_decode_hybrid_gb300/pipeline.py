@@ -88,19 +88,54 @@ class SpecStep:
 
     LAUNCHES_PER_STEP = 3
 
+    # -- the replay-commit variant (chains): no checkpoints, re-run k tokens --
+    def verify_nockpt(self, stream=None):
+        G.gdn_verify_span_nockpt(self.dims, self.n_tok, self.x, self.a, self.b, self.conv_w,
+                                 self.ssm_state, self.conv_state, self.out, stream)
+
+    def commit_replay(self, stream=None):
+        G.gdn_commit_replay(self.dims, self.n_tok, self.accept_len, self.x, self.a, self.b, self.conv_w,
+                            self.ssm_state, self.conv_state, self.dev_status, stream)
+
+    def step_replay(self, stream=None):
+        """verify (no checkpoints) -> accept -> replay the accepted tokens."""
+        self.verify_nockpt(stream)
+        self.accept(stream)
+        self.commit_replay(stream)
+
+    LAUNCHES_PER_STEP_REPLAY = 4
+
+    def replay_bytes(self, accept_len: np.ndarray) -> int:
+        """Algorithmic bytes of one replay-variant step: the verify reads the
+        state and inputs and writes o; the replay reads and writes the state of
+        every request with k > 0 and reads its k tokens' inputs."""
+        s = self.shape
+        el = 2 if s.dtype == GDN_BF16 else 4
+        T, C, K = s.n_tok, s.conv_ch, s.conv_k
+        state = s.h_v * s.d_v * s.d_k * 4 + C * (K - 1) * 4
+        verify = s.batch * s.layers * (state + T * C * el + 2 * T * s.h_v * el + T * s.h_v * s.d_v * 4) \
+            + s.layers * C * K * el
+        rep = 0
+        for k in np.asarray(accept_len).tolist():
+            if k > 0:
+                rep += s.layers * (2 * state + k * C * el + 2 * k * s.h_v * el + C * K * el)
+        return verify + self.accept_bytes() + rep
+
     # -- the same step as one CUDA graph ------------------------------------
-    def capture(self):
-        """Capture verify -> accept -> restore into a CUDA graph over this
-        object's fixed buffers and shapes, so that a step is one graph launch
-        (no per-kernel launch gaps). One eager step runs first, outside the
-        capture, so that every kernel attribute is already set."""
-        self.step()
+    def capture(self, replay_commit: bool = False):
+        """Capture verify -> accept -> restore (or, with replay_commit, the
+        replay-commit step) into a CUDA graph over this object's fixed buffers
+        and shapes, so that a step is one graph launch (no per-kernel launch
+        gaps). One eager step runs first, outside the capture, so that every
+        kernel attribute is already set."""
+        fn = self.step_replay if replay_commit else self.step
+        fn()
         torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.graph(g, stream=s):
-            self.step(stream=s)
+            fn(stream=s)
         torch.cuda.current_stream(self.device).wait_stream(s)
         self._graph = g
         return g
@@ -173,6 +208,8 @@ def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None, graph: 
             h2d += host[name].numel() * host[name].element_size()
     if graph:
         st.replay()
+    elif getattr(st, "replay_commit", False):
+        st.step_replay(stream)
     else:
         st.step(stream)
     d2h = 0

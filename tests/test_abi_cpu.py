@@ -168,3 +168,29 @@ def test_restore_validation(lib):
     assert call(ck=None) == G.GDN_ERR_NULL
     assert call(st=FAKE + 8) == G.GDN_ERR_ALIGN
     assert call(cc=FAKE + 8) == G.GDN_ERR_ALIGN
+
+
+def test_replay_entry_points_validate_before_launch(lib):
+    d = _dims()
+    f = lib.gdn_verify_span_nockpt
+    assert f(ctypes.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == G.GDN_ERR_DIMS
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None) == G.GDN_ERR_NULL
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, None) == G.GDN_ERR_ALIGN
+    g = lib.gdn_commit_replay
+    assert g(None, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
+    assert g(ctypes.byref(d), 65, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_DIMS
+    assert g(ctypes.byref(d), 4, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
+    assert g(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, FAKE, None, None) == G.GDN_ERR_ALIGN
+    assert g(ctypes.byref(d), 4, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_ALIGN
+
+
+def test_topk_validation(lib):
+    ws = G.spec_topk_workspace_bytes(4, 8)
+    assert ws > 0 and G.spec_topk_workspace_bytes(4, 33) == 0 and G.spec_topk_workspace_bytes(0, 8) == 0
+    f = lib.spec_topk
+    assert f(4, 100, 0, FAKE, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_DIMS
+    assert f(4, 100, 33, FAKE, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_DIMS
+    assert f(4, 7, 8, FAKE, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_DIMS
+    assert f(4, 100, 8, None, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_NULL
+    assert f(4, 100, 8, FAKE + 4, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_ALIGN
+    assert f(4, 100, 8, FAKE, FAKE, FAKE, FAKE, ws - 8, None, None) == G.GDN_ERR_WORKSPACE

@@ -284,7 +284,7 @@ def test_accept_all_match_and_token_range():
     am, kl, kn, ds, ws = accept_only(logits, tokens)
     assert list(kl) == [L, 8] and list(kn) == [L, 8]
     assert ds & G.GDN_DEV_TOKEN_RANGE
-    assert int(ws.count_nonzero().item()) > 0  # keys stay; counters are back to zero
+    assert int(ws.count_nonzero().item()) == 0  # keys and counters are back to zero
     expect_oracle(logits, tokens, None, am, kl, kn)
 
 
@@ -438,3 +438,86 @@ def test_host_buffer_step_matches_device_step():
     am, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0])
     assert int(out["accept_len"][0]) == kl == 2 and int(out["accept_node"][0]) == kn
     np.testing.assert_array_equal(out["argmax"][0].numpy(), am)
+
+
+# ------------------------------------------------------------ replay-commit variant
+
+def test_verify_without_checkpoints_matches_and_writes_none():
+    wl = W.make_workload(1, seed=70)
+    a = run(wl, restore=False)
+    b = SpecStep(wl)
+    b.ssm_ckpt.fill_(-7.0)
+    b.conv_ckpt.fill_(-7.0)
+    b.verify_nockpt()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out, b.out)
+    assert bool((b.ssm_ckpt == -7.0).all()) and bool((b.conv_ckpt == -7.0).all())
+
+
+@pytest.mark.parametrize("wid,layers", [(1, None), (2, 3), (0, None)])
+def test_replay_commit_equals_checkpoint_restore(wid, layers):
+    """Replaying the first k tokens from the live state gives, bit for bit,
+    the state that restoring checkpoint k gives (k = 0 leaves it alone)."""
+    wl = W.make_workload(wid, seed=71, **({} if layers is None else {"layers": layers}))
+    ref = run(wl, restore=False)
+    T = wl.shape.n_tok
+    for k in sorted({0, 1, min(2, T), T // 2, T}):
+        st = SpecStep(wl)
+        st.accept_len.fill_(k)
+        st.commit_replay()
+        torch.cuda.synchronize()
+        if k == 0:
+            want_s = torch.from_numpy(wl.ssm0).cuda()
+            want_c = torch.from_numpy(wl.conv0).cuda()
+        else:
+            want_s = ref.ssm_ckpt[:, :, k - 1]
+            want_c = ref.conv_ckpt[:, :, k - 1]
+        assert torch.equal(st.ssm_state, want_s), k
+        assert torch.equal(st.conv_state, want_c), k
+        assert int(st.dev_status.item()) == 0
+
+
+def test_replay_variant_step_vs_oracle_and_range_flag():
+    wl = W.make_workload(2, seed=9, layers=2)
+    st = SpecStep(wl)
+    st.step_replay()
+    torch.cuda.synchronize()
+    am, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0])
+    assert int(st.accept_len[0]) == kl == 2
+    for y in range(2):
+        ck, cc, out = oracle.verify_request(wl, 0, layers=[y])[0]
+        assert slice_rel_err(st.ssm_state[0, y].cpu().numpy(), ck[kl - 1], 128 * 128) <= TOL
+        np.testing.assert_array_equal(st.conv_state[0, y].cpu().numpy(), cc[kl - 1].astype(np.float32))
+        assert slice_rel_err(st.out[0, y].cpu().numpy(), out, 128) <= TOL
+    before = st.ssm_state.clone()
+    st.accept_len.fill_(wl.shape.n_tok + 3)
+    st.dev_status.zero_()
+    st.commit_replay()
+    torch.cuda.synchronize()
+    assert torch.equal(before, st.ssm_state)
+    assert int(st.dev_status.item()) & G.GDN_DEV_NODE_RANGE
+
+
+def test_accept_workspace_shared_across_shapes():
+    """One workspace for calls whose counter and key regions overlap (batch
+    sizes crossing the 64-request counter block): every call leaves it zero."""
+    g = np.random.default_rng(35)
+    dev = torch.device("cuda")
+    wsb = G.spec_accept_workspace_bytes(300, 17)
+    ws = torch.zeros((wsb,), dtype=torch.uint8, device=dev)
+    for B in (3, 300, 70, 1, 200):
+        N, V = 17, 3000
+        logits = g.standard_normal((B, N, V)).astype(np.float32)
+        tokens = g.integers(0, V, (B, N)).astype(np.int32)
+        lg = torch.from_numpy(logits).to(dev)
+        tk = torch.from_numpy(tokens).to(dev)
+        am = torch.empty((B, N), dtype=torch.int32, device=dev)
+        kl = torch.empty((B,), dtype=torch.int32, device=dev)
+        kn = torch.empty((B,), dtype=torch.int32, device=dev)
+        G.spec_accept_greedy(B, N, V, lg, tk, None, am, kl, kn, ws, wsb)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero().item()) == 0
+        for r in (0, B - 1):
+            o = oracle.accept_greedy(logits[r], tokens[r])
+            np.testing.assert_array_equal(am[r].cpu().numpy(), o[0])
+            assert (int(kl[r]), int(kn[r])) == o[1:]
