@@ -32,10 +32,11 @@
 //    on-chip compute; its state loads are issued first and overlap it.
 //    Items whose staging does not fit in shared memory (long f32 spans) use
 //    the one-item-per-CTA kernel, which loads its inputs directly.
-//  * Tree: nodes run in index order; when parent(i) != i-1 each thread
+//  * Tree: nodes run in depth-first preorder (children in index order);
+//    when a node's parent is not the node just processed, each thread
 //    reloads its rows of the parent's checkpoint, which it wrote itself
 //    (same thread, same addresses: program order makes it visible; the
-//    slot is still in L2).
+//    slot is still in L2). Outputs stay indexed by node.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -115,7 +116,7 @@ __host__ __device__ inline Layout make_layout(int T, int DK, int K) {
     L.a = off; off = al16(off + (size_t)T * 4);
     L.b = off; off = al16(off + (size_t)T * 4);
     L.kq = off; off = al16(off + (size_t)T * 4);
-    L.par = off; off = al16(off + (size_t)(T + 1) * 4);
+    L.par = off; off = al16(off + (size_t)(2 * T + 1) * 4);  // parents, then the DFS order
     L.src = off; off = al16(off + (size_t)T * K * 4);
     L.total = off;
     return L;
@@ -145,6 +146,28 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
         par_s[i] = v;
     }
     __syncthreads();
+    if (tid == 0) {
+        // depth-first preorder of nodes 1..T, children in index order: a
+        // node's state is then mostly still in registers when its first
+        // child runs, and a parent state is reloaded only on a branch switch
+        int *ord_s = par_s + (T + 1);
+        int first[GDN_MAX_TOKENS + 1], next[GDN_MAX_TOKENS + 1];
+        for (int i = 0; i <= T; ++i) first[i] = next[i] = -1;
+        for (int i = T; i >= 1; --i) {
+            next[i] = first[par_s[i]];
+            first[par_s[i]] = i;
+        }
+        int n = first[0], q = 0;
+        while (n > 0 && q < T) {
+            ord_s[q++] = n;
+            if (first[n] > 0) {
+                n = first[n];
+            } else {
+                while (n > 0 && next[n] < 0) n = par_s[n];
+                n = n > 0 ? next[n] : -1;
+            }
+        }
+    }
     for (int i = tid + 1; i <= T; i += blockDim.x) {
         int depth = 0;
         for (int n = i; n > 0; n = par_s[n]) ++depth;
@@ -222,18 +245,20 @@ __device__ __forceinline__ void load_rows(RowState<DK> &rs, const float *src, bo
 
 // One node t of the recurrence for this thread's rows: one checkpoint slot.
 // s_in: the item's initial rows; ck0: slot 0 of the item's rows.
+// `prev` is the node whose state the registers hold (0: the initial state).
 template <int DK, bool TREE>
-__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK> &rs, int t, const float *s_in,
-                                               float *ck0, const float *q_s, const float *k_s,
-                                               const float *v_s, float *o_s, const float *a_s,
-                                               const float *b_s, const float *kq_s, const int *par_s) {
+__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK> &rs, int t, int prev,
+                                               const float *s_in, float *ck0, const float *q_s,
+                                               const float *k_s, const float *v_s, float *o_s,
+                                               const float *a_s, const float *b_s, const float *kq_s,
+                                               const int *par_s) {
     constexpr int NV4 = RowState<DK>::NV4;
     const int lane = threadIdx.x & 31;
     const int j8 = lane & (kLanesPerRow - 1);
     const size_t slot = (size_t)p.H_v * p.d_v * DK;
     if constexpr (TREE) {
         const int pp = par_s[t + 1];
-        if (pp != t) {
+        if (pp != prev) {
             const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
 #pragma unroll
             for (int s = 0; s < kSlots; ++s)
@@ -293,8 +318,18 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK> &rs
                                           float *ck0, const float *q_s, const float *k_s,
                                           const float *v_s, float *o_s, const float *a_s,
                                           const float *b_s, const float *kq_s, const int *par_s) {
-    for (int t = 0; t < p.T; ++t)
-        recurrence_step<DK, TREE>(p, rs, t, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+    if constexpr (TREE) {
+        const int *ord_s = par_s + (p.T + 1);  // depth-first order of the nodes
+        int prev = 0;
+        for (int q = 0; q < p.T; ++q) {
+            const int node = ord_s[q];
+            recurrence_step<DK, TREE>(p, rs, node - 1, prev, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+            prev = node;
+        }
+    } else {
+        for (int t = 0; t < p.T; ++t)
+            recurrence_step<DK, TREE>(p, rs, t, t, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+    }
 }
 
 // o of one item, from shared memory [T][kRowsPerCta] to out[b][y][t][h][row]
@@ -542,7 +577,7 @@ __host__ __device__ inline PipeLayout make_pipe_layout(int T, int DK, int K, int
     L.a = off; off = al16(off + (size_t)T * 4);
     L.b = off; off = al16(off + (size_t)T * 4);
     L.kq = off; off = al16(off + (size_t)T * 4);
-    L.par = off; off = al16(off + (size_t)(T + 1) * 4);
+    L.par = off; off = al16(off + (size_t)(2 * T + 1) * 4);  // parents, then the DFS order
     L.src = off; off = al16(off + (size_t)T * K * 4);
     L.xst = off; off = al16(off + (size_t)T * XS * esize);
     L.wst = off; off = al16(off + XS * K * esize);
@@ -580,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     if (it >= n_items) return;
     float ga = 0.f, gb = 0.f;
     int pr = 0;
+    int tables_of = -1;  // request whose tree tables are in shared memory
     {
         const Item I0 = decode_item(p, it, nrb);
         prefetch_item<DK, BF16>(p, I0, xst, wst, cst);
@@ -599,8 +635,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         }
         __syncthreads();  // staged inputs and gates visible to every thread
         if constexpr (TREE) {
-            tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s);
-            __syncthreads();
+            if (I.bidx != tables_of) {  // the tables depend on the request only
+                tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s);
+                __syncthreads();
+                tables_of = I.bidx;
+            }
         }
 
         // conv1d + SiLU from the staged inputs. Work unit = (channel, half of
@@ -776,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
     if (has_rows) {
         const float *s_in = p.ssm_out + head_off;
         for (int t = 0; t < Te; ++t)
-            recurrence_step<DK, false>(p, rs, t, s_in, nullptr, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, nullptr);
+            recurrence_step<DK, false>(p, rs, t, t, s_in, nullptr, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, nullptr);
         const int lane = tid & 31, j8 = lane & (kLanesPerRow - 1);
 #pragma unroll
         for (int s2 = 0; s2 < kSlots; ++s2)
