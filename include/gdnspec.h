@@ -84,8 +84,9 @@ typedef void *gdn_stream_t;
 #define GDN_DEV_TOKEN_RANGE 0x1   /* a draft token id outside [0, vocab): counted as a mismatch */
 #define GDN_DEV_NAN_LOGIT 0x2     /* a NaN logit was seen: it ranks above every number */
 #define GDN_DEV_NODE_RANGE 0x4    /* accepted node outside [0, n_tok]: nothing restored for it */
-#define GDN_DEV_TREE 0x8          /* a device parent array broke parent[i] in [0, i): that node
-                                     was skipped (outputs for it are zero / unmatched) */
+#define GDN_DEV_TREE 0x8          /* a device parent array broke parent[i] in [0, i): the kernel
+                                     used parent i-1 for that node (verify) or left it unmatched
+                                     (acceptance) instead of reading out of bounds */
 
 /* Limits of this library. */
 #define GDN_MAX_TOKENS 64         /* n_tok (= N - 1) per span */
@@ -129,13 +130,16 @@ typedef struct gdn_dims {
  *   out       [B][Y][n_tok][h_v][d_v]       f32 o_t
  * The live state (ssm_in, conv_in) is never written: rejecting every token
  * needs no work. Outputs must not overlap inputs.
+ *   dev_status  nullable, device int32 for device-side findings, as in
+ *               gdn_tree_verify (a chain defines none today; it is accepted so
+ *               both verify calls take the same arguments).
  * Returns GDN_OK or GDN_ERR_{NULL,DIMS,ALIGN,DTYPE,CUDA}.
  */
 int gdn_verify_span(const gdn_dims *dims, int32_t n_tok,
                     const void *x, const void *a, const void *b, const void *conv_w,
                     const float *ssm_in, const float *conv_in,
                     float *ssm_ckpt, float *conv_ckpt, float *out,
-                    gdn_stream_t stream);
+                    int32_t *dev_status, gdn_stream_t stream);
 
 /*
  * gdn_tree_verify — verify a DDTree of n_nodes nodes (node 0 = committed
@@ -262,7 +266,7 @@ int gdn_rollback_restore(const gdn_dims *dims, int32_t n_tok,
 int gdn_verify_span_nockpt(const gdn_dims *dims, int32_t n_tok,
                            const void *x, const void *a, const void *b, const void *conv_w,
                            const float *ssm_in, const float *conv_in, float *out,
-                           gdn_stream_t stream);
+                           int32_t *dev_status, gdn_stream_t stream);
 
 /*
  * gdn_commit_replay — for every request b with k = accept_len_dev[b] in

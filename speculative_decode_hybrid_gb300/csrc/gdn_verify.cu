@@ -134,10 +134,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // depth(i) - (K-1-j) when that is >= 1, else conv-state slot K-2 + that
 // depth (encoded -1 - slot). pg is the request's parent array in global
 // memory; `pr` is pg[tid] already loaded by this thread (when tid <= T).
+__device__ __forceinline__ void bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// tid / nthreads: this thread's rank in the calling group; the group syncs
+// on hardware barrier `bar` (0 with the whole block = __syncthreads).
 __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *pg, int pr, int *par_s,
-                                            int *src_s) {
-    const int T = p.T, K = p.K, tid = threadIdx.x;
-    for (int i = tid; i <= T; i += blockDim.x) {
+                                            int *src_s, int tid, int nthreads, int bar) {
+    const int T = p.T, K = p.K;
+    for (int i = tid; i <= T; i += nthreads) {
         int v = i == 0 ? -1 : (i == tid ? pr : pg[i]);
         if (i > 0 && (v < 0 || v >= i)) {
             v = i - 1;
@@ -145,7 +151,7 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
         }
         par_s[i] = v;
     }
-    __syncthreads();
+    bar_sync(bar, nthreads);
     if (tid == 0) {
         // depth-first preorder of nodes 1..T, children in index order: a
         // node's state is then mostly still in registers when its first
@@ -168,7 +174,7 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
             }
         }
     }
-    for (int i = tid + 1; i <= T; i += blockDim.x) {
+    for (int i = tid + 1; i <= T; i += nthreads) {
         int depth = 0;
         for (int n = i; n > 0; n = par_s[n]) ++depth;
         int node = i;
@@ -186,9 +192,10 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
 
 // Per-head L2 norm of q and k, q scale, k.q; one warp per node.
 template <int DK>
-__device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s, int count) {
+__device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s, int count,
+                                       int warp, int nwarps) {
     constexpr int PER = DK / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31;
     for (int t = warp; t < count; t += nwarps) {
         float qv[PER], kv[PER];
         float sq = 0.f, sk = 0.f;
@@ -334,9 +341,10 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK> &rs
 
 // o of one item, from shared memory [T][kRowsPerCta] to out[b][y][t][h][row]
 // with 16-byte stores (d_v, row0 and R are multiples of 16).
-__device__ __forceinline__ void write_out(const VerifyArgs &p, const Item &I, const float *o_s) {
+__device__ __forceinline__ void write_out(const VerifyArgs &p, const Item &I, const float *o_s, int tid,
+                                          int nthreads) {
     const int r4 = I.R / 4;
-    for (int i = threadIdx.x; i < p.T * r4; i += blockDim.x) {
+    for (int i = tid; i < p.T * r4; i += nthreads) {
         const int t = i / r4, r = (i - t * r4) * 4;
         st4(p.out + (((size_t)I.by * p.T + t) * p.H_v + I.h) * p.d_v + I.row0 + r,
             ld4(o_s + (size_t)t * kRowsPerCta + r));
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
     if constexpr (TREE) {
         const int32_t *pg = p.parent + (size_t)I.bidx * (T + 1);
         const int pr = tid <= T ? (tid == 0 ? -1 : pg[tid]) : 0;
-        tree_tables(p, pg, pr, par_s, src_s);
+        tree_tables(p, pg, pr, par_s, src_s, tid, nthreads, 0);
     }
     for (int t = tid; t < T; t += nthreads) {
         const size_t gi = ((size_t)I.by * T + t) * p.H_v + I.h;
@@ -477,14 +485,14 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
         }
     }
     __syncthreads();
-    norm_qk<DK>(p, q_s, k_s, kq_s, p.T);
+    norm_qk<DK>(p, q_s, k_s, kq_s, p.T, threadIdx.x >> 5, blockDim.x >> 5);
     __syncthreads();
     if (has_rows) {
         float *ck0 = p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
         recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
     }
     __syncthreads();
-    write_out(p, I, o_s);
+    write_out(p, I, o_s, threadIdx.x, blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -497,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
 // offset is a multiple of 16 bytes, see the host-side eligibility check).
 template <int DK, bool BF16>
 __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I, unsigned char *xst,
-                                              unsigned char *wst, unsigned char *cst) {
+                                              unsigned char *wst, unsigned char *cst, int tid, int nthreads) {
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int XS = 2 * DK + kRowsPerCta;
-    const int T = p.T, K = p.K, tid = threadIdx.x, nthreads = blockDim.x;
+    const int T = p.T, K = p.K;
     const unsigned char *xg = static_cast<const unsigned char *>(p.x);
     const unsigned char *wg = static_cast<const unsigned char *>(p.w);
     const unsigned char *cg = reinterpret_cast<const unsigned char *>(p.conv_in);
@@ -550,8 +558,8 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
 // and, for trees, the parent array (thread i <= T); loaded into registers.
 template <bool BF16, bool TREE>
 __device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item &I, float &ga, float &gb,
-                                                 int &pr) {
-    const int T = p.T, tid = threadIdx.x;
+                                                 int &pr, int tid) {
+    const int T = p.T;
     if (tid < T) {
         const size_t gi = ((size_t)I.by * T + tid) * p.H_v + I.h;
         ga = ld_in<BF16>(p.a, gi);
@@ -586,6 +594,92 @@ __host__ __device__ inline PipeLayout make_pipe_layout(int T, int DK, int K, int
     return L;
 }
 
+// conv1d + SiLU of item I from its staged inputs, by threads tid of nthreads.
+// Work unit = (channel, half of the nodes), consecutive threads on
+// consecutive channels (coalesced conv-checkpoint stores, conflict-free
+// staging reads). A chain keeps its K-window in registers (one staged load
+// per output); a tree gathers each node's window along its root path.
+template <int DK, bool BF16, bool TREE, int KT>
+__device__ __forceinline__ void conv_staged(const VerifyArgs &p, const Item &I, const unsigned char *xst,
+                                            const unsigned char *wst, const unsigned char *cst,
+                                            const int *src_s, float *q_s, float *k_s, float *v_s, int tid,
+                                            int nthreads) {
+    constexpr int XS = 2 * DK + kRowsPerCta;
+    constexpr int KM = KT > 0 ? KT : GDN_MAX_CONV_K;
+    const int T = p.T, K = KT > 0 ? KT : p.K;
+    const float *cstf = reinterpret_cast<const float *>(cst);
+    const size_t cc_tok = (size_t)p.C * (K - 1);
+    {
+        const int nch = 2 * DK + I.R;
+        const bool own_qk = (I.h % (p.H_v / p.H_k) == 0) && I.rb == 0;
+        const int nchunk = T >= 8 ? 2 : 1;
+        const int tc = (T + nchunk - 1) / nchunk;
+        for (int u = tid; u < nch * nchunk; u += nthreads) {
+            const int lc = u % nch, tb = (u / nch) * tc, te = min(T, tb + tc);
+            float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
+            const int stride = lc < 2 * DK ? DK : kRowsPerCta;
+            const bool own = (lc >= 2 * DK || own_qk) && p.conv_ckpt != nullptr;
+            float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)item_channel<DK>(p, I, lc) * (K - 1);
+            float wr[KM];
+#pragma unroll
+            for (int j = 0; j < KM; ++j) wr[j] = j < K ? ld_in<BF16>(wst, (size_t)lc * K + j) : 0.f;
+            if constexpr (!TREE) {
+                // win[j], j < K-1: sequence position tb-(K-1)+j (x row when >= 0,
+                // else conv-state slot K-1+position)
+                float win[KM];
+#pragma unroll
+                for (int j = 0; j < KM; ++j) {
+                    win[j] = 0.f;
+                    if (j < K - 1) {
+                        const int sp = tb - (K - 1) + j;
+                        win[j] = sp >= 0 ? ld_in<BF16>(xst, (size_t)sp * XS + lc)
+                                         : cstf[(size_t)lc * (K - 1) + (K - 1 + sp)];
+                    }
+                }
+                for (int t = tb; t < te; ++t) {
+                    const float xv = ld_in<BF16>(xst, (size_t)t * XS + lc);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < KM; ++j)
+                        if (j < K) acc = fmaf(wr[j], j < K - 1 ? win[j] : xv, acc);
+                    dst[(size_t)t * stride] = silu(acc);
+#pragma unroll
+                    for (int j = 0; j < KM - 1; ++j) {
+                        if (j < K - 2) win[j] = win[j + 1];
+                        else if (j == K - 2) win[j] = xv;
+                    }
+                    if (own) {
+#pragma unroll
+                        for (int j = 0; j < KM - 1; ++j)
+                            if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j];
+                    }
+                }
+            } else {
+                for (int t = tb; t < te; ++t) {
+                    float win[KM];
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < KM; ++j) {
+                        win[j] = 0.f;
+                        if (j < K) {
+                            const int sn = src_s[t * K + j];  // >= 1: node; else -1 - conv-state slot
+                            win[j] = sn >= 1 ? ld_in<BF16>(xst, (size_t)(sn - 1) * XS + lc)
+                                             : cstf[(size_t)lc * (K - 1) + (-1 - sn)];
+                            acc = fmaf(wr[j], win[j], acc);
+                        }
+                    }
+                    dst[(size_t)t * stride] = silu(acc);
+                    if (own) {
+#pragma unroll
+                        for (int j = 0; j < KM - 1; ++j)
+                            if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j + 1];
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Persistent kernel: CTAs walk the items round-robin; while an item streams
 // its checkpoints, the next item's inputs are copied into the staging
 // buffers, so its prologue is on-chip compute only.
@@ -618,8 +712,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     int tables_of = -1;  // request whose tree tables are in shared memory
     {
         const Item I0 = decode_item(p, it, nrb);
-        prefetch_item<DK, BF16>(p, I0, xst, wst, cst);
-        prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr);
+        prefetch_item<DK, BF16>(p, I0, xst, wst, cst, tid, nthreads);
+        prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr, tid);
     }
     while (true) {
         const Item I = decode_item(p, it, nrb);
@@ -636,95 +730,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         __syncthreads();  // staged inputs and gates visible to every thread
         if constexpr (TREE) {
             if (I.bidx != tables_of) {  // the tables depend on the request only
-                tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s);
+                tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0);
                 __syncthreads();
                 tables_of = I.bidx;
             }
         }
 
-        // conv1d + SiLU from the staged inputs. Work unit = (channel, half of
-        // the nodes), consecutive threads on consecutive channels (coalesced
-        // conv-checkpoint stores, conflict-free staging reads). A chain keeps
-        // its K-window in registers (one staged load per output); a tree
-        // gathers each node's window along its root path.
-        {
-            const int nch = 2 * DK + I.R;
-            const bool own_qk = (I.h % (p.H_v / p.H_k) == 0) && I.rb == 0;
-            const int nchunk = T >= 8 ? 2 : 1;
-            const int tc = (T + nchunk - 1) / nchunk;
-            for (int u = tid; u < nch * nchunk; u += nthreads) {
-                const int lc = u % nch, tb = (u / nch) * tc, te = min(T, tb + tc);
-                float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
-                const int stride = lc < 2 * DK ? DK : kRowsPerCta;
-                const bool own = (lc >= 2 * DK || own_qk) && p.conv_ckpt != nullptr;
-                float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)item_channel<DK>(p, I, lc) * (K - 1);
-                float wr[KM];
-#pragma unroll
-                for (int j = 0; j < KM; ++j) wr[j] = j < K ? ld_in<BF16>(wst, (size_t)lc * K + j) : 0.f;
-                if constexpr (!TREE) {
-                    // win[j], j < K-1: sequence position tb-(K-1)+j (x row when >= 0,
-                    // else conv-state slot K-1+position)
-                    float win[KM];
-#pragma unroll
-                    for (int j = 0; j < KM; ++j) {
-                        win[j] = 0.f;
-                        if (j < K - 1) {
-                            const int sp = tb - (K - 1) + j;
-                            win[j] = sp >= 0 ? ld_in<BF16>(xst, (size_t)sp * XS + lc)
-                                             : cstf[(size_t)lc * (K - 1) + (K - 1 + sp)];
-                        }
-                    }
-                    for (int t = tb; t < te; ++t) {
-                        const float xv = ld_in<BF16>(xst, (size_t)t * XS + lc);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int j = 0; j < KM; ++j)
-                            if (j < K) acc = fmaf(wr[j], j < K - 1 ? win[j] : xv, acc);
-                        dst[(size_t)t * stride] = silu(acc);
-#pragma unroll
-                        for (int j = 0; j < KM - 1; ++j) {
-                            if (j < K - 2) win[j] = win[j + 1];
-                            else if (j == K - 2) win[j] = xv;
-                        }
-                        if (own) {
-#pragma unroll
-                            for (int j = 0; j < KM - 1; ++j)
-                                if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j];
-                        }
-                    }
-                } else {
-                    for (int t = tb; t < te; ++t) {
-                        float win[KM];
-                        float acc = 0.f;
-#pragma unroll
-                        for (int j = 0; j < KM; ++j) {
-                            win[j] = 0.f;
-                            if (j < K) {
-                                const int sn = src_s[t * K + j];  // >= 1: node; else -1 - conv-state slot
-                                win[j] = sn >= 1 ? ld_in<BF16>(xst, (size_t)(sn - 1) * XS + lc)
-                                                 : cstf[(size_t)lc * (K - 1) + (-1 - sn)];
-                                acc = fmaf(wr[j], win[j], acc);
-                            }
-                        }
-                        dst[(size_t)t * stride] = silu(acc);
-                        if (own) {
-#pragma unroll
-                            for (int j = 0; j < KM - 1; ++j)
-                                if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j + 1];
-                        }
-                    }
-                }
-            }
-        }
+        conv_staged<DK, BF16, TREE, KT>(p, I, xst, wst, cst, src_s, q_s, k_s, v_s, tid, nthreads);
         __syncthreads();  // staging consumed; q, k, v ready
 
         const int next = it + gridDim.x;
         if (next < n_items) {
             const Item In = decode_item(p, next, nrb);
-            prefetch_item<DK, BF16>(p, In, xst, wst, cst);
-            prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr);
+            prefetch_item<DK, BF16>(p, In, xst, wst, cst, tid, nthreads);
+            prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
         }
-        norm_qk<DK>(p, q_s, k_s, kq_s, p.T);
+        norm_qk<DK>(p, q_s, k_s, kq_s, p.T, threadIdx.x >> 5, blockDim.x >> 5);
         __syncthreads();
         if (has_rows) {
             float *ck0 =
@@ -732,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
         }
         __syncthreads();
-        write_out(p, I, o_s);
+        write_out(p, I, o_s, threadIdx.x, blockDim.x);
         if (next >= n_items) break;
         it = next;
     }
@@ -810,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
         }
     }
     __syncthreads();
-    norm_qk<DK>(p, q_s, k_s, kq_s, Te);
+    norm_qk<DK>(p, q_s, k_s, kq_s, Te, threadIdx.x >> 5, blockDim.x >> 5);
     __syncthreads();
     if (has_rows) {
         const float *s_in = p.ssm_out + head_off;
@@ -964,11 +985,12 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
 extern "C" int gdn_verify_span(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
                                const void *b, const void *conv_w, const float *ssm_in,
                                const float *conv_in, float *ssm_ckpt, float *conv_ckpt, float *out,
-                               gdn_stream_t stream) {
+                               int32_t *dev_status, gdn_stream_t stream) {
     int rc = check_common(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out);
     if (rc != GDN_OK) return rc;
+    if (dev_status && !gdnhost::aligned_to(dev_status, 4)) return GDN_ERR_ALIGN;
     const VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt,
-                                   out, nullptr, nullptr);
+                                   out, nullptr, dev_status);
     return dispatch_verify<false>(d, v, static_cast<cudaStream_t>(stream));
 }
 
@@ -993,7 +1015,8 @@ extern "C" int gdn_tree_verify(const gdn_dims *d, int32_t n_nodes, const int32_t
 
 extern "C" int gdn_verify_span_nockpt(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
                                       const void *b, const void *conv_w, const float *ssm_in,
-                                      const float *conv_in, float *out, gdn_stream_t stream) {
+                                      const float *conv_in, float *out, int32_t *dev_status,
+                                      gdn_stream_t stream) {
     int rc = gdnhost::check_dims(d, n_tok);
     if (rc != GDN_OK) return rc;
     if (!x || !a || !b || !conv_w || !ssm_in || !out) return GDN_ERR_NULL;
@@ -1004,8 +1027,9 @@ extern "C" int gdn_verify_span_nockpt(const gdn_dims *d, int32_t n_tok, const vo
     if (!aligned_to(x, es) || !aligned_to(a, es) || !aligned_to(b, es) || !aligned_to(conv_w, es))
         return GDN_ERR_ALIGN;
     if (!aligned16(ssm_in) || !aligned16(out) || (d->conv_k > 1 && !aligned16(conv_in))) return GDN_ERR_ALIGN;
+    if (dev_status && !aligned_to(dev_status, 4)) return GDN_ERR_ALIGN;
     const VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, nullptr, nullptr, out,
-                                   nullptr, nullptr);
+                                   nullptr, dev_status);
     return dispatch_verify<false>(d, v, static_cast<cudaStream_t>(stream));
 }
 

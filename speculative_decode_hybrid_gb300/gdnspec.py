@@ -85,7 +85,7 @@ def load(path: Optional[str] = None):
         lib = ctypes.CDLL(p)
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         dp = ctypes.POINTER(gdn_dims)
-        lib.gdn_verify_span.argtypes = [dp, i32] + [vp] * 9 + [vp]
+        lib.gdn_verify_span.argtypes = [dp, i32] + [vp] * 9 + [vp, vp]
         lib.gdn_tree_verify.argtypes = [dp, i32, vp, vp] + [vp] * 9 + [vp, vp]
         lib.spec_accept_greedy.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         lib.spec_accept_workspace_bytes.argtypes = [i32, i32]
@@ -94,7 +94,7 @@ def load(path: Optional[str] = None):
         lib.spec_topk.argtypes = [i32, i32, i32, vp, vp, vp, vp, sz, vp, vp]
         lib.spec_topk_workspace_bytes.argtypes = [i32, i32]
         lib.spec_topk_workspace_bytes.restype = sz
-        lib.gdn_verify_span_nockpt.argtypes = [dp, i32] + [vp] * 7 + [vp]
+        lib.gdn_verify_span_nockpt.argtypes = [dp, i32] + [vp] * 7 + [vp, vp]
         lib.gdn_commit_replay.argtypes = [dp, i32] + [vp] * 9
         lib.gdn_tree_check.argtypes = [vp, i32, i32, i32, i32]
         lib.gdn_status_str.argtypes = [ctypes.c_int]
@@ -142,10 +142,10 @@ def _ok(rc: int, what: str):
 
 
 def gdn_verify_span(dims: gdn_dims, n_tok: int, x, a, b, conv_w, ssm_in, conv_in,
-                    ssm_ckpt, conv_ckpt, out, stream=None) -> None:
+                    ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None) -> None:
     rc = load().gdn_verify_span(ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b), _ptr(conv_w),
                                 _ptr(ssm_in), _ptr(conv_in), _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out),
-                                _stream(stream))
+                                _ptr(dev_status), _stream(stream))
     _ok(rc, "gdn_verify_span")
 
 
@@ -185,10 +185,10 @@ def gdn_rollback_restore(dims: gdn_dims, n_tok: int, accept_node_dev, ssm_ckpt, 
 
 
 def gdn_verify_span_nockpt(dims: gdn_dims, n_tok: int, x, a, b, conv_w, ssm_in, conv_in, out,
-                           stream=None) -> None:
+                           dev_status=None, stream=None) -> None:
     rc = load().gdn_verify_span_nockpt(ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b),
                                        _ptr(conv_w), _ptr(ssm_in), _ptr(conv_in), _ptr(out),
-                                       _stream(stream))
+                                       _ptr(dev_status), _stream(stream))
     _ok(rc, "gdn_verify_span_nockpt")
 
 

@@ -69,7 +69,7 @@ class SpecStep:
         else:
             G.gdn_verify_span(self.dims, self.n_tok, self.x, self.a, self.b, self.conv_w,
                               self.ssm_state, self.conv_state, self.ssm_ckpt, self.conv_ckpt,
-                              self.out, stream)
+                              self.out, self.dev_status, stream)
 
     def accept(self, stream=None):
         s = self.shape
@@ -91,7 +91,7 @@ class SpecStep:
     # -- the replay-commit variant (chains): no checkpoints, re-run k tokens --
     def verify_nockpt(self, stream=None):
         G.gdn_verify_span_nockpt(self.dims, self.n_tok, self.x, self.a, self.b, self.conv_w,
-                                 self.ssm_state, self.conv_state, self.out, stream)
+                                 self.ssm_state, self.conv_state, self.out, self.dev_status, stream)
 
     def commit_replay(self, stream=None):
         G.gdn_commit_replay(self.dims, self.n_tok, self.accept_len, self.x, self.a, self.b, self.conv_w,

@@ -87,7 +87,8 @@ def _verify(lib, dims, n_tok, **ptrs):
     p = dict(x=FAKE, a=FAKE, b=FAKE, w=FAKE, ssm_in=FAKE, conv_in=FAKE, ck=FAKE, cc=FAKE, out=FAKE)
     p.update(ptrs)
     return lib.gdn_verify_span(ctypes.byref(dims) if dims is not None else None, n_tok, p["x"], p["a"],
-                               p["b"], p["w"], p["ssm_in"], p["conv_in"], p["ck"], p["cc"], p["out"], None)
+                               p["b"], p["w"], p["ssm_in"], p["conv_in"], p["ck"], p["cc"], p["out"],
+                               p.get("ds"), None)
 
 
 @pytest.mark.parametrize("bad", [
@@ -110,6 +111,7 @@ def test_verify_rejects_before_launch(lib):
     for name in ("ssm_in", "ck", "out", "conv_in", "cc"):
         assert _verify(lib, _dims(), 4, **{name: FAKE + 4}) == G.GDN_ERR_ALIGN, name
     assert _verify(lib, _dims(in_dtype=G.GDN_BF16), 4, x=FAKE + 1) == G.GDN_ERR_ALIGN
+    assert _verify(lib, _dims(), 4, ds=FAKE + 2) == G.GDN_ERR_ALIGN
     # K == 1 needs no conv buffers, but still validates everything else
     assert _verify(lib, _dims(conv_k=1, d_v=72), 4, conv_in=None, cc=None) == G.GDN_ERR_DIMS
 
@@ -173,9 +175,10 @@ def test_restore_validation(lib):
 def test_replay_entry_points_validate_before_launch(lib):
     d = _dims()
     f = lib.gdn_verify_span_nockpt
-    assert f(ctypes.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == G.GDN_ERR_DIMS
-    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None) == G.GDN_ERR_NULL
-    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, None) == G.GDN_ERR_ALIGN
+    assert f(ctypes.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_DIMS
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, None, None) == G.GDN_ERR_ALIGN
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None) == G.GDN_ERR_ALIGN
     g = lib.gdn_commit_replay
     assert g(None, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
     assert g(ctypes.byref(d), 65, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_DIMS
