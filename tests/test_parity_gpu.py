@@ -117,6 +117,7 @@ EDGE_SHAPES = {
     "gqa4_dk64_bf16": shape(h_k=1, h_v=4, d_k=64, d_v=128),
     "vocab_odd": shape(vocab=1001),
     "vocab_tiny": shape(vocab=3, n_nodes=9),
+    "wide_dv_four_row_blocks": shape(h_k=1, h_v=2, d_v=512, n_nodes=5, layers=1),
 }
 
 
