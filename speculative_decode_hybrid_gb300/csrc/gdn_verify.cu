@@ -25,11 +25,14 @@
 //    v channels for all nodes into shared memory, L2 norms, gates. The conv
 //    checkpoint (the last K-1 inputs) is a shifted copy of the inputs and is
 //    written by the item that owns the channels.
-//  * Persistent kernel (the default): 2 CTAs per SM walk the items
-//    round-robin. While an item streams its checkpoints, cp.async copies the
-//    next item's inputs (x tile, conv taps, conv state) into shared memory and
-//    its gates / parent array into registers, so the next prologue is pure
-//    on-chip compute; its state loads are issued first and overlap it.
+//  * Work-stealing kernel (the default): one CTA per item, 2 resident per
+//    SM; a running CTA takes the item of a CTA that has not started yet by
+//    cancelling that CTA's launch (cluster launch control), so the items run
+//    in index order and a CTA on a slow SM simply runs fewer of them. While
+//    an item streams its checkpoints, cp.async copies the next item's inputs
+//    (x tile, conv taps, conv state) into shared memory and its gates /
+//    parent array into registers, so the next prologue is pure on-chip
+//    compute; its state loads are issued first and overlap it.
 //    Items whose staging does not fit in shared memory (long f32 spans) use
 //    the one-item-per-CTA kernel, which loads its inputs directly.
 //  * Tree: nodes run in depth-first preorder (children in index order);
@@ -58,6 +61,7 @@ constexpr int kRowsPerCta = kRowsPerWarp * kMaxWarps;  // 128
 constexpr int kColStride = 4 * kLanesPerRow;           // lane j owns columns 4j + kColStride*m + 0..3
 constexpr int kThreads = kMaxWarps * 32;
 constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kStaticSmem = 64;  // the work-stealing kernel's static shared memory
 static_assert(kRowsPerWarp <= 16 && 16 % kRowsPerWarp == 0, "d_v is validated as a multiple of 16");
 
 struct VerifyArgs {
@@ -128,6 +132,61 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Cluster launch control (sm_100 family): a running CTA asks the hardware to
+// cancel the launch of a CTA of the same grid that has not started; on
+// success it gets that CTA's index and does its work. The 16-byte response
+// lands in shared memory and completes a transaction on an mbarrier. A
+// request is never issued again after one has failed. One thread (the
+// leader) drives all of it.
+// ---------------------------------------------------------------------------
+constexpr unsigned kStealPolls = 1u << 22;  // bound on the response wait
+
+__device__ __forceinline__ void steal_init(unsigned bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+// Ask for the next pending CTA. The response buffer was last read through
+// the generic proxy; the proxy fence orders that read before the
+// asynchronous write of the new response.
+__device__ __forceinline__ void steal_issue(unsigned resp, unsigned bar) {
+    asm volatile(
+        "fence.proxy.async.shared::cta;\n\t"
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], 16;" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Wait for the response of phase `phase` (bounded); then the x index of the
+// cancelled CTA, or -1 when the request failed (nothing left to take), or -2
+// when the wait gave up.
+__device__ __forceinline__ int steal_result(unsigned resp, unsigned bar, unsigned phase) {
+    unsigned done = 0;
+    for (unsigned i = 0; i < kStealPolls && !done; ++i)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(phase)
+            : "memory");
+    if (!done) return -2;
+    unsigned long long lo, hi;
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(resp) : "memory");
+    int ok = 0, x = -1;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "mov.b128 r, {%2, %3};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "+r"(x)
+        : "l"(lo), "l"(hi)
+        : "memory");
+    return ok ? x : -1;
+}
 
 // Tree: validated parents -> par_s, and the conv-window table src_s:
 // position j of node i's window holds the input of the node at path depth
@@ -685,20 +744,21 @@ __device__ __forceinline__ void conv_staged(const VerifyArgs &p, const Item &I, 
     }
 }
 
-// Persistent kernel: CTAs walk the items in rounds of the grid; while an
-// item streams its checkpoints, the next item's inputs are copied into the
-// staging buffers, so its prologue is on-chip compute only. Consecutive items
-// of a CTA that share a key head (the value heads of one GQA group, and the
-// row blocks of one head) reuse the q/k conv and norms already in shared
-// memory: only the v channels are staged and convolved again.
+// Work-stealing kernel: one CTA per item (grid = n_items); a running CTA
+// cancels the launch of the next pending CTA and runs its item, so the items
+// run in index order (the CTAs in flight write neighbouring checkpoint rows)
+// and the load balances itself across SMs whose store bandwidth differs.
+// While an item streams its checkpoints, the next item's inputs are copied
+// into the staging buffers, so its prologue is on-chip compute only. When a
+// CTA's next item shares the key head of the current one (another value head
+// of the GQA group, or another row block), the q/k conv and norms already in
+// shared memory are reused: only the v channels are staged and convolved.
 //
 // KT: the conv width as a compile-time constant (4 for Qwen3.5/3.6), or 0 to
 // read it from the arguments.
 template <int DK, bool BF16, bool TREE, int KT>
 __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const VerifyArgs p, int n_items) {
     constexpr int ES = BF16 ? 2 : 4;
-    constexpr int XS = 2 * DK + kRowsPerCta;
-    constexpr int KM = KT > 0 ? KT : GDN_MAX_CONV_K;  // unrolled window width
     extern __shared__ __align__(16) unsigned char smem[];
     const int T = p.T, K = KT > 0 ? KT : p.K;
     const PipeLayout L = make_pipe_layout(T, DK, K, ES);
@@ -708,26 +768,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     float *kq_s = reinterpret_cast<float *>(smem + L.kq);
     int *par_s = reinterpret_cast<int *>(smem + L.par), *src_s = reinterpret_cast<int *>(smem + L.src);
     unsigned char *xst = smem + L.xst, *wst = smem + L.wst, *cst = smem + L.cst;
-    const float *cstf = reinterpret_cast<const float *>(cst);
     const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
-    const size_t cc_tok = (size_t)p.C * (K - 1);
 
-    // Round-robin walk: round k of the grid runs slots k*G .. k*G+G-1, so
-    // the CTAs in flight together write neighbouring checkpoint rows (a
-    // contiguous block per CTA instead ran 13% slower on GB300). Slots map to
-    // items so that gs consecutive rounds of a CTA take the gs items of one
-    // key head (gs = value heads per key head x row blocks), which then share
-    // the q/k conv; slots past the last full group of rounds map to
-    // themselves.
-    const int G = gridDim.x;
-    const int gs = (p.H_v / p.H_k) * nrb;
-    const long long grouped = (long long)(n_items / G / gs) * gs * G;
-    auto item_of = [&](int slot) -> int {
-        if (slot >= grouped) return slot;
-        const int k = slot / G, c = slot - k * G, j = k / gs;
-        return (j * G + c) * gs + (k - j * gs);
-    };
+    // work stealing: this CTA's own item first, then items of cancelled CTAs
+    __shared__ __align__(16) unsigned long long steal_s[3];  // response (16 B), mbarrier
+    __shared__ int next_s;
+    const unsigned resp = (unsigned)__cvta_generic_to_shared(steal_s);
+    const unsigned bar = resp + 16;
+    unsigned phase = 0;
+    bool stealing = true;  // the last request succeeded
+    if (tid == 0) steal_init(bar);
     int it = blockIdx.x;
     if (it >= n_items) return;
     float ga = 0.f, gb = 0.f;
@@ -735,12 +786,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     int tables_of = -1;  // request whose tree tables are in shared memory
     bool reuse_qk = false;  // q_s / k_s / kq_s hold this item's normalised q, k
     {
-        const Item I0 = decode_item(p, item_of(it), nrb);
+        const Item I0 = decode_item(p, it, nrb);
         prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads);
         prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr, tid);
     }
     while (true) {
-        const Item I = decode_item(p, item_of(it), nrb);
+        if (tid == 0 && stealing) steal_issue(resp, bar);  // the next item, answered during this prologue
+        const Item I = decode_item(p, it, nrb);
         const bool has_rows = warp * kRowsPerWarp < I.R;
         const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
         RowState<DK> rs;
@@ -761,12 +813,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         }
 
         conv_staged<DK, BF16, TREE, KT>(p, I, xst, wst, cst, src_s, q_s, k_s, v_s, reuse_qk, tid, nthreads);
-        __syncthreads();  // staging consumed; q, k, v ready
+        if (tid == 0) {
+            int nx = -1;
+            if (stealing) {
+                nx = steal_result(resp, bar, phase);
+                phase ^= 1u;
+                if (nx == -2 && p.dev_status) atomicOr(p.dev_status, GDN_DEV_SCHED);
+                if (nx < 0 || nx >= n_items) stealing = false;
+            }
+            next_s = nx;
+        }
+        __syncthreads();  // staging consumed; q, k, v ready; next_s set
 
-        const int next = it + G;
+        const int next = next_s >= 0 && next_s < n_items ? next_s : n_items;
         bool next_reuse = false;
         if (next < n_items) {
-            const Item In = decode_item(p, item_of(next), nrb);
+            const Item In = decode_item(p, next, nrb);
             next_reuse = In.by == I.by && In.g == I.g;
             prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads);
             prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
@@ -917,26 +979,13 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     const int threads = rows / kRowsPerWarp * 32;
     const PipeLayout Lp = make_pipe_layout(a.T, DK, a.K, BF16 ? 2 : 4);
     // the persistent kernel keeps one gate / parent value per thread in registers
-    if (aligned_inputs && Lp.total <= kMaxSmem && threads > a.T) {
+    if (aligned_inputs && Lp.total + kStaticSmem <= kMaxSmem && threads > a.T) {
         auto kern = a.K == 4 ? gdn_verify_persistent<DK, BF16, TREE, 4> : gdn_verify_persistent<DK, BF16, TREE, 0>;
         static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
         std::atomic<size_t> &set = a.K == 4 ? set4 : set0;
         if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
-        // resident CTAs per SM, looked up once per (threads, shared memory)
-        // so that a step captured into a CUDA graph makes no queries
-        static std::atomic<unsigned long long> occ_key{0};
-        static std::atomic<int> occ_val{0};
-        const unsigned long long key = ((unsigned long long)Lp.total << 16) | (unsigned)threads | (a.K == 4 ? 1ull << 15 : 0);
-        int per_sm = occ_key.load(std::memory_order_acquire) == key ? occ_val.load(std::memory_order_relaxed) : 0;
-        if (per_sm == 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, Lp.total) != cudaSuccess)
-                return GDN_ERR_CUDA;
-            occ_val.store(per_sm, std::memory_order_relaxed);
-            occ_key.store(key, std::memory_order_release);
-        }
-        const int sms = gdnhost::sm_count();
-        int grid = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
-        if (grid > n_items) grid = n_items;
+        // one CTA per item: the running CTAs take the pending ones' items
+        const int grid = n_items;
         kern<<<grid, threads, Lp.total, stream>>>(a, n_items);
     } else {
         auto kern = gdn_verify_kernel<DK, BF16, TREE>;

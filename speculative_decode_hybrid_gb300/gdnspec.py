@@ -36,6 +36,7 @@ GDN_DEV_TOKEN_RANGE = 0x1
 GDN_DEV_NAN_LOGIT = 0x2
 GDN_DEV_NODE_RANGE = 0x4
 GDN_DEV_TREE = 0x8
+GDN_DEV_SCHED = 0x10
 
 GDN_MAX_TOKENS = 64
 GDN_MAX_CONV_K = 8
