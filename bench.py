@@ -41,7 +41,10 @@ METRIC = "GDN verify+rollback tokens·layers/s (span 16, 48 layers); % of HBM ro
 UNIT = "tokens*layers/s"
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
-VERIFY_SRC = os.path.join(ROOT, "speculative_decode_hybrid_gb300", "csrc", "gdn_verify.cu")
+# the verify kernel's sources, hashed together (in this order) to tie the
+# recorded ncu traffic to the code it was taken with
+VERIFY_SRCS = [os.path.join(ROOT, "speculative_decode_hybrid_gb300", "csrc", f)
+               for f in ("gdn_verify.cu", "gdn_verify_parts.cuh", "gdn_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_verify_kernel_traffic.txt")
 
 
@@ -57,9 +60,10 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--commit", choices=["checkpoint", "replay"], default="checkpoint",
+    ap.add_argument("--commit", choices=["checkpoint", "replay", "wy"], default="checkpoint",
                     help="checkpoint: per-token checkpoints + restore (the method); replay: "
-                         "verify without checkpoints, then re-run the accepted tokens")
+                         "verify without checkpoints, then re-run the accepted tokens; wy: the "
+                         "replay variant with the span solved in chunked (WY) form")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -93,8 +97,11 @@ def recorded_traffic():
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
-        with open(VERIFY_SRC, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        h = hashlib.sha256()
+        for src in VERIFY_SRCS:
+            with open(src, "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()
         if vals.get("source_sha256") != sha:
             return None
         return int(vals["dram_bytes_per_launch"])
@@ -194,7 +201,7 @@ def config_of(st, wl, kl):
             "l2": "256 MiB buffer written between timed steps (outside the events); "
                   "step footprint %.2f GiB" % (st.verify_bytes() / 2 ** 30),
             "parallelism": "replicas (independent requests per rank, no collective)",
-            "commit": getattr(st, "replay_commit", False) and "replay" or "checkpoint"}
+            "commit": getattr(st, "commit", "checkpoint")}
 
 
 BENCH_WID = 2
@@ -220,13 +227,13 @@ def run_ours(args):
 
     wl = W.make_workload(BENCH_WID, seed=args.seed + 1000 * rank, layers=args.layers)
     st = SpecStep(wl, device=dev)
-    replay = args.commit == "replay"
+    replay = args.commit != "checkpoint"
     if replay and st.tree:
         raise SystemExit("the replay commit is defined for chains only")
-    st.replay_commit = replay
-    f_verify = st.verify_nockpt if replay else st.verify
-    f_commit = st.commit_replay if replay else st.restore
-    step_fn = st.step_replay if replay else st.step
+    st.commit = args.commit
+    f_verify = {"checkpoint": st.verify, "replay": st.verify_nockpt, "wy": st.verify_wy}[args.commit]
+    f_commit = {"checkpoint": st.restore, "replay": st.commit_replay, "wy": st.commit_wy}[args.commit]
+    step_fn = st.step_fn(args.commit)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ssm0 = st.ssm_state.clone()
@@ -277,7 +284,7 @@ def run_ours(args):
     #      events around every replay, L2 flushed between replays
     graph_ok = True
     try:
-        st.capture(replay_commit=replay)
+        st.capture(args.commit)
         for _ in range(3):
             st.replay()
         torch.cuda.synchronize(dev)
@@ -329,7 +336,9 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(st, wl, kl),
         "roofline": {"bound": "hbm",
-                     "kernel": "gdn_verify_persistent (%s)" % ("gdn_verify_span_nockpt" if replay else "gdn_verify_span"),
+                     "kernel": {"checkpoint": "gdn_verify_persistent (gdn_verify_span)",
+                                "replay": "gdn_verify_persistent (gdn_verify_span_nockpt)",
+                                "wy": "gdn_wy_kernel (gdn_verify_span_wy)"}[args.commit],
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": peak_kind, "traffic": None if replay else recorded_traffic(),
                      "algorithmic_bytes_per_launch": vbytes,
@@ -342,7 +351,8 @@ def run_ours(args):
         "mode": "cuda_graph" if graph_ok else "eager",
         "eager": {"value": eager_value, "ms_per_step": eager_max_ms / K},
         "clocks": clocks,
-        "gpu_launches": (SpecStep.LAUNCHES_PER_STEP_REPLAY if replay else SpecStep.LAUNCHES_PER_STEP) * K,
+        "gpu_launches": {"checkpoint": SpecStep.LAUNCHES_PER_STEP, "replay": SpecStep.LAUNCHES_PER_STEP_REPLAY,
+                         "wy": SpecStep.LAUNCHES_PER_STEP_WY}[args.commit] * K,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

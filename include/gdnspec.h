@@ -95,6 +95,7 @@ typedef void *gdn_stream_t;
 #define GDN_MAX_TOKENS 64         /* n_tok (= N - 1) per span */
 #define GDN_MAX_CONV_K 8
 #define GDN_MAX_TOPK 32           /* k of spec_topk */
+#define GDN_WY_MAX_TOKENS 16      /* n_tok of the chunked-form calls */
 
 /*
  * Model and batch dimensions shared by the verify and restore calls.
@@ -285,6 +286,38 @@ int gdn_commit_replay(const gdn_dims *dims, int32_t n_tok, const int32_t *accept
                       const void *x, const void *a, const void *b, const void *conv_w,
                       float *ssm_state, float *conv_state, int32_t *dev_status,
                       gdn_stream_t stream);
+
+/*
+ * gdn_verify_span_wy — gdn_verify_span_nockpt computed in chunked (WY) form:
+ * per (request, layer, value head) the span's tokens are solved together
+ * (one S_0 [K | Q] product, a shared T x T unit lower triangular forward
+ * substitution) instead of one rank-1 update per token. Same arguments,
+ * layouts and results (up to rounding order) as gdn_verify_span_nockpt.
+ * (lucebox PR #506, Summary: the span's gated delta rule; openinfer PR #626,
+ * Summary: the conservative commit this verify pairs with.)
+ * Limits: n_tok <= GDN_WY_MAX_TOKENS; x and conv_w 16-byte aligned.
+ * Returns GDN_OK or GDN_ERR_{NULL,DIMS,ALIGN,DTYPE,CUDA}.
+ */
+int gdn_verify_span_wy(const gdn_dims *dims, int32_t n_tok,
+                       const void *x, const void *a, const void *b, const void *conv_w,
+                       const float *ssm_in, const float *conv_in, float *out,
+                       int32_t *dev_status, gdn_stream_t stream);
+
+/*
+ * gdn_commit_wy — gdn_commit_replay in chunked form: for every request b with
+ * k = accept_len_dev[b] in [1, n_tok], the live state becomes
+ * A_{k-1} S + sum_{j<k} D[k-1][j] b_j u_j k_j^T (the state after token k-1,
+ * u from the same forward substitution as gdn_verify_span_wy) and the live
+ * conv state the last K-1 inputs; k = 0 leaves the request untouched; k
+ * outside [0, n_tok] changes nothing and sets GDN_DEV_NODE_RANGE. Same
+ * arguments and layouts as gdn_commit_replay; two kernels on `stream`.
+ * Limits: n_tok <= GDN_WY_MAX_TOKENS; x and conv_w 16-byte aligned.
+ * Returns GDN_OK or GDN_ERR_{NULL,DIMS,ALIGN,DTYPE,CUDA}.
+ */
+int gdn_commit_wy(const gdn_dims *dims, int32_t n_tok, const int32_t *accept_len_dev,
+                  const void *x, const void *a, const void *b, const void *conv_w,
+                  float *ssm_state, float *conv_state, int32_t *dev_status,
+                  gdn_stream_t stream);
 
 /*
  * spec_topk — the k best logits of each row in the greedy order: larger value

@@ -41,11 +41,12 @@ GDN_DEV_SCHED = 0x10
 GDN_MAX_TOKENS = 64
 GDN_MAX_CONV_K = 8
 GDN_MAX_TOPK = 32
+GDN_WY_MAX_TOKENS = 16
 
 EXPORTED = ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
             "spec_accept_workspace_bytes", "gdn_rollback_restore", "gdn_tree_check",
             "gdn_status_str", "gdn_verify_span_nockpt", "gdn_commit_replay", "spec_topk",
-            "spec_topk_workspace_bytes")
+            "spec_topk_workspace_bytes", "gdn_verify_span_wy", "gdn_commit_wy")
 
 
 class GdnError(RuntimeError):
@@ -97,12 +98,14 @@ def load(path: Optional[str] = None):
         lib.spec_topk_workspace_bytes.restype = sz
         lib.gdn_verify_span_nockpt.argtypes = [dp, i32] + [vp] * 7 + [vp, vp]
         lib.gdn_commit_replay.argtypes = [dp, i32] + [vp] * 9
+        lib.gdn_verify_span_wy.argtypes = [dp, i32] + [vp] * 7 + [vp, vp]
+        lib.gdn_commit_wy.argtypes = [dp, i32] + [vp] * 9
         lib.gdn_tree_check.argtypes = [vp, i32, i32, i32, i32]
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
         for f in ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
                   "gdn_rollback_restore", "gdn_tree_check", "gdn_verify_span_nockpt",
-                  "gdn_commit_replay", "spec_topk"):
+                  "gdn_commit_replay", "spec_topk", "gdn_verify_span_wy", "gdn_commit_wy"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -199,6 +202,22 @@ def gdn_commit_replay(dims: gdn_dims, n_tok: int, accept_len_dev, x, a, b, conv_
                                   _ptr(b), _ptr(conv_w), _ptr(ssm_state), _ptr(conv_state),
                                   _ptr(dev_status), _stream(stream))
     _ok(rc, "gdn_commit_replay")
+
+
+def gdn_verify_span_wy(dims: gdn_dims, n_tok: int, x, a, b, conv_w, ssm_in, conv_in, out,
+                       dev_status=None, stream=None) -> None:
+    rc = load().gdn_verify_span_wy(ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b),
+                                   _ptr(conv_w), _ptr(ssm_in), _ptr(conv_in), _ptr(out),
+                                   _ptr(dev_status), _stream(stream))
+    _ok(rc, "gdn_verify_span_wy")
+
+
+def gdn_commit_wy(dims: gdn_dims, n_tok: int, accept_len_dev, x, a, b, conv_w, ssm_state,
+                  conv_state, dev_status=None, stream=None) -> None:
+    rc = load().gdn_commit_wy(ctypes.byref(dims), int(n_tok), _ptr(accept_len_dev), _ptr(x), _ptr(a),
+                              _ptr(b), _ptr(conv_w), _ptr(ssm_state), _ptr(conv_state),
+                              _ptr(dev_status), _stream(stream))
+    _ok(rc, "gdn_commit_wy")
 
 
 def spec_topk_workspace_bytes(rows: int, k: int) -> int:

@@ -105,10 +105,38 @@ class SpecStep:
 
     LAUNCHES_PER_STEP_REPLAY = 4
 
+    # -- the same variant in chunked (WY) form --------------------------------
+    def verify_wy(self, stream=None):
+        G.gdn_verify_span_wy(self.dims, self.n_tok, self.x, self.a, self.b, self.conv_w,
+                             self.ssm_state, self.conv_state, self.out, self.dev_status, stream)
+
+    def commit_wy(self, stream=None):
+        G.gdn_commit_wy(self.dims, self.n_tok, self.accept_len, self.x, self.a, self.b, self.conv_w,
+                        self.ssm_state, self.conv_state, self.dev_status, stream)
+
+    def step_wy(self, stream=None):
+        """verify (chunked form, no checkpoints) -> accept -> commit the
+        accepted prefix in closed form."""
+        self.verify_wy(stream)
+        self.accept(stream)
+        self.commit_wy(stream)
+
+    LAUNCHES_PER_STEP_WY = 4
+
+    COMMITS = ("checkpoint", "replay", "wy")
+
+    def step_fn(self, commit: str = "checkpoint"):
+        """The step of a commit variant: "checkpoint" (verify with per-token
+        checkpoints -> accept -> restore), "replay" (rank-1 verify without
+        checkpoints -> accept -> replay of the accepted tokens) or "wy" (the
+        replay variant in chunked form)."""
+        return {"checkpoint": self.step, "replay": self.step_replay, "wy": self.step_wy}[commit]
+
     def replay_bytes(self, accept_len: np.ndarray) -> int:
-        """Algorithmic bytes of one replay-variant step: the verify reads the
-        state and inputs and writes o; the replay reads and writes the state of
-        every request with k > 0 and reads its k tokens' inputs."""
+        """Algorithmic bytes of one replay-variant step (either form): the
+        verify reads the state and inputs and writes o; the commit reads and
+        writes the state of every request with k > 0 and reads its k tokens'
+        inputs."""
         s = self.shape
         el = 2 if s.dtype == GDN_BF16 else 4
         T, C, K = s.n_tok, s.conv_ch, s.conv_k
@@ -122,13 +150,13 @@ class SpecStep:
         return verify + self.accept_bytes() + rep
 
     # -- the same step as one CUDA graph ------------------------------------
-    def capture(self, replay_commit: bool = False):
-        """Capture verify -> accept -> restore (or, with replay_commit, the
-        replay-commit step) into a CUDA graph over this object's fixed buffers
-        and shapes, so that a step is one graph launch (no per-kernel launch
-        gaps). One eager step runs first, outside the capture, so that every
-        kernel attribute is already set."""
-        fn = self.step_replay if replay_commit else self.step
+    def capture(self, commit: str = "checkpoint"):
+        """Capture the step of a commit variant (see step_fn) into a CUDA
+        graph over this object's fixed buffers and shapes, so that a step is
+        one graph launch (no per-kernel launch gaps). One eager step runs
+        first, outside the capture, so that every kernel attribute is already
+        set."""
+        fn = self.step_fn(commit)
         fn()
         torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
@@ -208,10 +236,8 @@ def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None, graph: 
             h2d += host[name].numel() * host[name].element_size()
     if graph:
         st.replay()
-    elif getattr(st, "replay_commit", False):
-        st.step_replay(stream)
     else:
-        st.step(stream)
+        st.step_fn(getattr(st, "commit", "checkpoint"))(stream)
     d2h = 0
     for name in ("accept_len", "accept_node", "argmax"):
         out_host[name].copy_(getattr(st, name), non_blocking=True)

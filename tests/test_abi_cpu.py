@@ -187,6 +187,28 @@ def test_replay_entry_points_validate_before_launch(lib):
     assert g(ctypes.byref(d), 4, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_ALIGN
 
 
+def test_wy_entry_points_validate_before_launch(lib):
+    d = _dims()
+    f = lib.gdn_verify_span_wy
+    assert f(ctypes.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_DIMS
+    assert f(ctypes.byref(d), G.GDN_WY_MAX_TOKENS + 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+             None) == G.GDN_ERR_DIMS
+    assert f(ctypes.byref(d), G.GDN_WY_MAX_TOKENS, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+             None) == G.GDN_ERR_NULL
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
+    assert f(ctypes.byref(d), 4, FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_ALIGN
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE + 8, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_ALIGN
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, None, None) == G.GDN_ERR_ALIGN
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None) == G.GDN_ERR_ALIGN
+    g = lib.gdn_commit_wy
+    assert g(None, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
+    assert g(ctypes.byref(d), G.GDN_WY_MAX_TOKENS + 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+             None) == G.GDN_ERR_DIMS
+    assert g(ctypes.byref(d), 4, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_NULL
+    assert g(ctypes.byref(d), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, FAKE, None, None) == G.GDN_ERR_ALIGN
+    assert g(ctypes.byref(d), 4, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == G.GDN_ERR_ALIGN
+
+
 def test_topk_validation(lib):
     ws = G.spec_topk_workspace_bytes(4, 8)
     assert ws > 0 and G.spec_topk_workspace_bytes(4, 33) == 0 and G.spec_topk_workspace_bytes(0, 8) == 0

@@ -522,3 +522,111 @@ def test_accept_workspace_shared_across_shapes():
             o = oracle.accept_greedy(logits[r], tokens[r])
             np.testing.assert_array_equal(am[r].cpu().numpy(), o[0])
             assert (int(kl[r]), int(kn[r])) == o[1:]
+
+
+# ------------------------------------------------------------ chunked (WY) form of the replay variant
+
+WY_NAMES = ["workload0", "workload1", "two_row_blocks_ragged", "min_rows_f32_one_token", "conv_k1",
+            "conv_k2", "conv_k8", "ratio1_batch3", "gqa4_dk64_bf16", "wide_dv_four_row_blocks"]
+
+
+def wy_workload(name, seed):
+    if name == "workload0":
+        return W.make_workload(0, seed=seed)
+    if name == "workload1":
+        return W.make_workload(1, seed=seed)
+    return W.draw(EDGE_SHAPES[name], seed=seed + zlib.crc32(name.encode()) % 1000)
+
+
+@pytest.mark.parametrize("name", WY_NAMES)
+def test_wy_verify_vs_oracle(name):
+    """o of the chunked form against the oracle's token-by-token recurrence,
+    and next to the rank-1 kernel's; the live state is left untouched."""
+    wl = wy_workload(name, 80)
+    s = wl.shape
+    st = SpecStep(wl)
+    st.verify_wy()
+    torch.cuda.synchronize()
+    out_wy = st.out.clone()
+    assert torch.equal(st.ssm_state.cpu(), torch.from_numpy(wl.ssm0))
+    st.verify_nockpt()
+    torch.cuda.synchronize()
+    for r in range(s.batch):
+        refs = oracle.verify_request(wl, r)
+        for y, (ck, cc, out) in enumerate(refs):
+            e = slice_rel_err(out_wy[r, y].cpu().numpy(), out, s.d_v)
+            assert e <= TOL, (name, r, y, e)
+            assert slice_rel_err(out_wy[r, y].cpu().numpy(), st.out[r, y].cpu().numpy(), s.d_v) <= TOL
+    assert int(st.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("name", WY_NAMES)
+def test_wy_commit_vs_oracle(name):
+    """The live state after the chunked commit of k tokens is the oracle's
+    checkpoint k-1 (within TOL; the conv state bit for bit); k = 0 leaves
+    the request untouched. Requests take different k."""
+    wl = wy_workload(name, 81)
+    s = wl.shape
+    T = s.n_tok
+    refs = {r: oracle.verify_request(wl, r) for r in range(s.batch)}
+    for k0 in sorted({0, 1, min(2, T), T // 2, T}):
+        ks = [(k0 + r) % (T + 1) for r in range(s.batch)]
+        st = SpecStep(wl)
+        st.accept_len.copy_(torch.tensor(ks, dtype=torch.int32))
+        st.commit_wy()
+        torch.cuda.synchronize()
+        for r, k in enumerate(ks):
+            for y in range(s.layers):
+                g_s = st.ssm_state[r, y].cpu().numpy()
+                g_c = st.conv_state[r, y].cpu().numpy()
+                if k == 0:
+                    np.testing.assert_array_equal(g_s, wl.ssm0[r, y])
+                    np.testing.assert_array_equal(g_c, wl.conv0[r, y])
+                    continue
+                ck, cc, _ = refs[r][y]
+                e = slice_rel_err(g_s, ck[k - 1], s.d_v * s.d_k)
+                assert e <= TOL, (name, k, r, y, e)
+                if s.conv_k > 1:
+                    np.testing.assert_array_equal(g_c, cc[k - 1].astype(np.float32))
+        assert int(st.dev_status.item()) == 0
+
+
+def test_wy_step_vs_oracle_graph_and_range_flag():
+    wl = W.make_workload(2, seed=9, layers=2)
+    st = SpecStep(wl)
+    st.step_wy()
+    torch.cuda.synchronize()
+    am, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0])
+    assert int(st.accept_len[0]) == kl == 2
+    for y in range(2):
+        ck, cc, out = oracle.verify_request(wl, 0, layers=[y])[0]
+        assert slice_rel_err(st.ssm_state[0, y].cpu().numpy(), ck[kl - 1], 128 * 128) <= TOL
+        np.testing.assert_array_equal(st.conv_state[0, y].cpu().numpy(), cc[kl - 1].astype(np.float32))
+        assert slice_rel_err(st.out[0, y].cpu().numpy(), out, 128) <= TOL
+    # the captured step gives the eager step's bytes
+    a, b = SpecStep(wl), SpecStep(wl)
+    a.step_wy()
+    a.step_wy()
+    b.capture("wy")  # one eager step, then the capture
+    b.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a.ssm_state, b.ssm_state) and torch.equal(a.conv_state, b.conv_state)
+    assert torch.equal(a.out, b.out)
+    # k out of range: nothing changes, the flag is set
+    before = st.ssm_state.clone()
+    st.accept_len.fill_(wl.shape.n_tok + 3)
+    st.dev_status.zero_()
+    st.commit_wy()
+    torch.cuda.synchronize()
+    assert torch.equal(before, st.ssm_state)
+    assert int(st.dev_status.item()) & G.GDN_DEV_NODE_RANGE
+
+
+def test_wy_rejects_long_spans():
+    wl = W.draw(EDGE_SHAPES["max_tokens"], seed=5)
+    st = SpecStep(wl)
+    with pytest.raises(G.GdnError) as ei:
+        st.verify_wy()
+    assert ei.value.status == G.GDN_ERR_DIMS
+    with pytest.raises(G.GdnError):
+        st.commit_wy()
