@@ -64,6 +64,8 @@ def parse():
                     help="checkpoint: per-token checkpoints + restore (the method); replay: "
                          "verify without checkpoints, then re-run the accepted tokens; wy: the "
                          "replay variant with the span solved in chunked (WY) form")
+    ap.add_argument("--per-layer-steps", type=int, default=200,
+                    help="steps of the per-layer launch measurement (batch 1, checkpoint commit)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -327,6 +329,12 @@ def run_ours(args):
     if args.e2e_steps > 0:
         e2e = run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl)
 
+    # ---- the same step with one verify launch per layer (how a model whose
+    #      layers run in sequence calls it), as a CUDA graph; batch 1 only
+    per_layer = None
+    if args.commit == "checkpoint" and st.shape.batch == 1 and graph_ok and args.per_layer_steps > 0:
+        per_layer = run_per_layer(st, flush, dev, stream, min(K, args.per_layer_steps), units, ws)
+
     # the state moved every step; put the initial one back (not timed)
     st.ssm_state.copy_(ssm0)
     st.conv_state.copy_(conv0)
@@ -348,6 +356,7 @@ def run_ours(args):
                      "restore_us_mean": statistics.mean(res_ms) * 1e3,
                      "step_bytes": step_bytes, "step_gbs": step_gbs, "step_frac": step_gbs / hbm},
         "e2e": e2e,
+        "per_layer": per_layer,
         "mode": "cuda_graph" if graph_ok else "eager",
         "eager": {"value": eager_value, "ms_per_step": eager_max_ms / K},
         "clocks": clocks,
@@ -388,6 +397,41 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
     assert int(out_host["accept_len"][0]) == int(kl[0])
     return {"value": e2e_units / e2e_max_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s)}
+
+
+def run_per_layer(st, flush, dev, stream, K, units, ws):
+    """Graph-replayed steps whose verify is one launch per layer, with the L2
+    flushed between replays; plus the per-layer verify launches alone
+    (eager, events around the whole loop)."""
+    import torch
+    main_graph = getattr(st, "_graph", None)
+    st.capture("checkpoint-per-layer")
+    for _ in range(3):
+        st.replay()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        st.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    vev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(min(K, 50))]
+    for i in range(len(vev)):
+        flush.fill_(i & 0xFF)
+        vev[i][0].record(stream)
+        st.verify_per_layer()
+        vev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ver_ms = [a.elapsed_time(b) for a, b in vev]
+    st._graph = main_graph
+    total_max_ms, units_all = aggregate(sum(step_ms), units * K, ws, dev)
+    return {"value": units_all / (total_max_ms / 1e3), "unit": UNIT, "steps": K,
+            "ms_per_step": total_max_ms / K, "launches_per_step": st.shape.layers + 2,
+            "verify_us_mean": statistics.mean(ver_ms) * 1e3,
+            "verify_us_per_layer": statistics.mean(ver_ms) * 1e3 / st.shape.layers,
+            "mode": "cuda_graph (step), eager (verify alone)"}
 
 
 def oracle_full_step(wl, layers, accept=True):

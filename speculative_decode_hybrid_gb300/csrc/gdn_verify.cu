@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
     float *kq_s = reinterpret_cast<float *>(smem + L.kq);
     int *par_s = reinterpret_cast<int *>(smem + L.par), *src_s = reinterpret_cast<int *>(smem + L.src);
     const int T = p.T, K = p.K;
-    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(p);
     const Item I = decode_item(p, (blockIdx.z * p.H_v + blockIdx.y) * nrb + blockIdx.x, nrb);
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
     const void *__restrict__ xin = p.x;
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     float *kq_s = reinterpret_cast<float *>(smem + L.kq);
     int *par_s = reinterpret_cast<int *>(smem + L.par), *src_s = reinterpret_cast<int *>(smem + L.src);
     unsigned char *xst = smem + L.xst, *wst = smem + L.wst, *cst = smem + L.cst;
-    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(p);
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
 
     // work stealing: this CTA's own item first, then items of cancelled CTAs
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
     float *a_s = reinterpret_cast<float *>(smem + L.a), *b_s = reinterpret_cast<float *>(smem + L.b);
     float *kq_s = reinterpret_cast<float *>(smem + L.kq);
     const int T = p.T, K = p.K;
-    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(p);
     const Item I = decode_item(p, (blockIdx.z * p.H_v + blockIdx.y) * nrb + blockIdx.x, nrb);
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
     const int Te = accept_len[I.bidx];
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
 
 template <int DK, bool BF16, bool TREE>
 int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStream_t stream) {
-    const int nrb = (a.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(a);
     const int n_items = batch * a.Y * a.H_v * nrb;
     const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;  // d_v % kRowsPerWarp == 0
     const int threads = rows / kRowsPerWarp * 32;
@@ -516,9 +516,18 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
         static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
         std::atomic<size_t> &set = a.K == 4 ? set4 : set0;
         if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
+        // Small launches (one layer, a few heads) split each head's rows into
+        // smaller blocks until there are items for about two resident CTAs
+        // per SM; every CTA still runs its item's whole conv prologue, and
+        // only the warps that own rows run the recurrence. Each row's
+        // arithmetic is the same whatever the block size.
+        VerifyArgs pa = a;
+        const int sms = gdnhost::sm_count();
+        const long long want = 2LL * (sms > 0 ? sms : 152);
+        while (pa.rpi > kRowsPerWarp && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
         // one CTA per item: the running CTAs take the pending ones' items
-        const int grid = n_items;
-        kern<<<grid, threads, Lp.total, stream>>>(a, n_items);
+        const int grid = batch * a.Y * a.H_v * row_blocks(pa);
+        kern<<<grid, threads, Lp.total, stream>>>(pa, grid);
     } else {
         auto kern = gdn_verify_kernel<DK, BF16, TREE>;
         static std::atomic<size_t> set{48 * 1024};
@@ -634,7 +643,7 @@ extern "C" int gdn_commit_replay(const gdn_dims *d, int32_t n_tok, const int32_t
                              nullptr, dev_status);
     v.ssm_out = ssm_state;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int nrb = (d->d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(v);
     const int rows = d->d_v < kRowsPerCta ? d->d_v : kRowsPerCta;
     const int threads = rows / kRowsPerWarp * 32;
     const Layout L = make_layout(n_tok, d->d_k, d->conv_k);

@@ -37,12 +37,16 @@ struct VerifyArgs {
     const int32_t *parent;  // [B][T+1] for trees, nullptr for chains
     int32_t *dev_status;
     float *ssm_out;         // replay commit: the live state, updated in place
+    int rpi;                // value rows per work item: a multiple of 16, <= kRowsPerCta
 };
 
 // One work item: (request*layer by, value head h, row block rb).
 struct Item {
     int by, h, rb, y, bidx, g, row0, R;
 };
+
+// Row blocks per value head.
+__host__ __device__ __forceinline__ int row_blocks(const VerifyArgs &p) { return (p.d_v + p.rpi - 1) / p.rpi; }
 
 __device__ __forceinline__ Item decode_item(const VerifyArgs &p, int it, int nrb) {
     Item I;
@@ -53,8 +57,8 @@ __device__ __forceinline__ Item decode_item(const VerifyArgs &p, int it, int nrb
     I.y = I.by % p.Y;
     I.bidx = I.by / p.Y;
     I.g = I.h / (p.H_v / p.H_k);  // key head floor(h * H_k / H_v)
-    I.row0 = I.rb * kRowsPerCta;
-    I.R = min(kRowsPerCta, p.d_v - I.row0);  // a multiple of kRowsPerWarp
+    I.row0 = I.rb * p.rpi;
+    I.R = min(p.rpi, p.d_v - I.row0);  // a multiple of kRowsPerWarp
     return I;
 }
 
@@ -486,6 +490,7 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
     v.parent = parent;
     v.dev_status = dev_status;
     v.ssm_out = nullptr;
+    v.rpi = kRowsPerCta;
     return v;
 }
 

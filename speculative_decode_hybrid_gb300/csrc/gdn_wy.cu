@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     float *kq_s = reinterpret_cast<float *>(smem + L.kq), *ac_s = reinterpret_cast<float *>(smem + L.ac);
     float *lm_s = reinterpret_cast<float *>(smem + L.lm), *mm_s = reinterpret_cast<float *>(smem + L.mm);
     float *dm_s = reinterpret_cast<float *>(smem + L.dm);
-    const int nrb = (p.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(p);
     const Item I = decode_item(p, blockIdx.x, nrb);
     const int tid = threadIdx.x, nthreads = blockDim.x;
 
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
 
 template <int DK, bool BF16, bool COMMIT>
 int launch_wy(const VerifyArgs &a, int batch, const int32_t *accept_len, cudaStream_t st) {
-    const int nrb = (a.d_v + kRowsPerCta - 1) / kRowsPerCta;
+    const int nrb = row_blocks(a);
     const long long n_items = (long long)batch * a.Y * a.H_v * nrb;
     if (n_items < 1 || n_items > 0x7fffffffLL) return GDN_ERR_DIMS;
     const WyLayout L = make_wy_layout(a.T, DK, a.K, BF16 ? 2 : 4);

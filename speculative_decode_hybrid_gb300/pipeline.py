@@ -123,6 +123,34 @@ class SpecStep:
 
     LAUNCHES_PER_STEP_WY = 4
 
+    # -- per-layer launches: how a model whose layers run in sequence calls it
+    def verify_per_layer(self, stream=None):
+        """The verify of each layer as its own launch (batch 1, where a
+        layer's slices of the [B][Y] layouts are contiguous)."""
+        s = self.shape
+        if s.batch != 1:
+            raise ValueError("per-layer launches are laid out for batch 1")
+        if not hasattr(self, "_dims1"):
+            self._dims1 = G.make_dims(1, 1, s.h_k, s.h_v, s.d_k, s.d_v, s.conv_k, s.dtype,
+                                      q_scale=self.dims.q_scale)
+        for y in range(s.layers):
+            if self.tree:
+                G.gdn_tree_verify(self._dims1, self.n_nodes, self.parent_host, self.parent, self.x[:, y],
+                                  self.a[:, y], self.b[:, y], self.conv_w[y], self.ssm_state[:, y],
+                                  self.conv_state[:, y], self.ssm_ckpt[:, y], self.conv_ckpt[:, y],
+                                  self.out[:, y], self.dev_status, stream)
+            else:
+                G.gdn_verify_span(self._dims1, self.n_tok, self.x[:, y], self.a[:, y], self.b[:, y],
+                                  self.conv_w[y], self.ssm_state[:, y], self.conv_state[:, y],
+                                  self.ssm_ckpt[:, y], self.conv_ckpt[:, y], self.out[:, y],
+                                  self.dev_status, stream)
+
+    def step_per_layer(self, stream=None):
+        """verify (one launch per layer) -> accept -> restore (all layers)."""
+        self.verify_per_layer(stream)
+        self.accept(stream)
+        self.restore(stream)
+
     COMMITS = ("checkpoint", "replay", "wy")
 
     def step_fn(self, commit: str = "checkpoint"):
@@ -130,7 +158,8 @@ class SpecStep:
         checkpoints -> accept -> restore), "replay" (rank-1 verify without
         checkpoints -> accept -> replay of the accepted tokens) or "wy" (the
         replay variant in chunked form)."""
-        return {"checkpoint": self.step, "replay": self.step_replay, "wy": self.step_wy}[commit]
+        return {"checkpoint": self.step, "replay": self.step_replay, "wy": self.step_wy,
+                "checkpoint-per-layer": self.step_per_layer}[commit]
 
     def replay_bytes(self, accept_len: np.ndarray) -> int:
         """Algorithmic bytes of one replay-variant step (either form): the

@@ -630,3 +630,16 @@ def test_wy_rejects_long_spans():
     assert ei.value.status == G.GDN_ERR_DIMS
     with pytest.raises(G.GdnError):
         st.commit_wy()
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_per_layer_launches_equal_one_launch(tree):
+    """One verify launch per layer gives, bit for bit, the all-layers launch."""
+    wl = W.make_workload(3 if tree else 2, seed=12, layers=3)
+    a, b = SpecStep(wl), SpecStep(wl)
+    a.verify()
+    b.verify_per_layer()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out, b.out)
+    assert torch.equal(a.ssm_ckpt, b.ssm_ckpt) and torch.equal(a.conv_ckpt, b.conv_ckpt)
+    assert int(b.dev_status.item()) == 0
