@@ -384,6 +384,14 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
     E = max(1, min(args.e2e_steps, K))
     e2e_s = []
     h2d = d2h = 0
+    mode = "eager copies + device graph"
+    try:
+        st.capture_host_step(host, out_host, args.commit)
+        mode = "one graph per step: x/a/b copied in 4 blocks, the verify of each block launched as " \
+               "its block lands, logits/tokens copied during the verify, then accept, commit, " \
+               "D2H of the result"
+    except Exception as exc:  # capture unsupported: copies stay eager around the device graph
+        print("host-step capture failed: %r" % (exc,), file=sys.stderr)
     for i in range(E + 3):
         flush.fill_(i & 0xFF)
         torch.cuda.synchronize(dev)
@@ -396,7 +404,8 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
     e2e_max_s, e2e_units = aggregate(sum(e2e_s), units * E, ws, dev)
     assert int(out_host["accept_len"][0]) == int(kl[0])
     return {"value": e2e_units / e2e_max_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s)}
+            "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s),
+            "mode": mode}
 
 
 def run_per_layer(st, flush, dev, stream, K, units, ws):

@@ -123,27 +123,61 @@ class SpecStep:
 
     LAUNCHES_PER_STEP_WY = 4
 
+    # -- verify over a block of requests x layers (contiguous slices) ------
+    def _dims_of(self, nb: int, ny: int):
+        cache = self.__dict__.setdefault("_sub_dims", {})
+        if (nb, ny) not in cache:
+            s = self.shape
+            cache[(nb, ny)] = G.make_dims(nb, ny, s.h_k, s.h_v, s.d_k, s.d_v, s.conv_k, s.dtype,
+                                          q_scale=self.dims.q_scale)
+        return cache[(nb, ny)]
+
+    def verify_block(self, b0: int, b1: int, y0: int, y1: int, kind: str = "checkpoint", stream=None):
+        """The verify of requests [b0, b1) x layers [y0, y1) as one launch.
+        The slices of the [B][Y] layouts must be contiguous: all layers, or
+        one request. kind: "checkpoint", "replay" (no checkpoints, rank-1)
+        or "wy" (no checkpoints, chunked form)."""
+        s = self.shape
+        if not (y0 == 0 and y1 == s.layers) and b1 - b0 != 1:
+            raise ValueError("a layer range is contiguous for one request only")
+        d = self._dims_of(b1 - b0, y1 - y0)
+        bs, ys = slice(b0, b1), slice(y0, y1)
+        x, a, b = self.x[bs, ys], self.a[bs, ys], self.b[bs, ys]
+        w, S, Cs = self.conv_w[ys], self.ssm_state[bs, ys], self.conv_state[bs, ys]
+        if not all(t.is_contiguous() for t in (x, a, b, w, S, Cs)):
+            raise ValueError("verify_block needs contiguous slices")
+        if kind == "checkpoint":
+            if self.tree:
+                G.gdn_tree_verify(d, self.n_nodes, self.parent_host[bs], self.parent[bs], x, a, b, w, S, Cs,
+                                  self.ssm_ckpt[bs, ys], self.conv_ckpt[bs, ys], self.out[bs, ys],
+                                  self.dev_status, stream)
+            else:
+                G.gdn_verify_span(d, self.n_tok, x, a, b, w, S, Cs, self.ssm_ckpt[bs, ys],
+                                  self.conv_ckpt[bs, ys], self.out[bs, ys], self.dev_status, stream)
+        elif kind == "replay":
+            G.gdn_verify_span_nockpt(d, self.n_tok, x, a, b, w, S, Cs, self.out[bs, ys], self.dev_status, stream)
+        else:
+            G.gdn_verify_span_wy(d, self.n_tok, x, a, b, w, S, Cs, self.out[bs, ys], self.dev_status, stream)
+
+    def blocks(self, n: int = 4):
+        """Up to n contiguous (b0, b1, y0, y1) blocks covering every request
+        and layer, in item order: layer ranges for one request, request
+        ranges otherwise."""
+        B, Y = self.shape.batch, self.shape.layers
+        if B == 1:
+            n = max(1, min(n, Y))
+            return [(0, 1, k * Y // n, (k + 1) * Y // n) for k in range(n)]
+        n = max(1, min(n, B))
+        return [(k * B // n, (k + 1) * B // n, 0, Y) for k in range(n)]
+
     # -- per-layer launches: how a model whose layers run in sequence calls it
     def verify_per_layer(self, stream=None):
         """The verify of each layer as its own launch (batch 1, where a
         layer's slices of the [B][Y] layouts are contiguous)."""
-        s = self.shape
-        if s.batch != 1:
+        if self.shape.batch != 1:
             raise ValueError("per-layer launches are laid out for batch 1")
-        if not hasattr(self, "_dims1"):
-            self._dims1 = G.make_dims(1, 1, s.h_k, s.h_v, s.d_k, s.d_v, s.conv_k, s.dtype,
-                                      q_scale=self.dims.q_scale)
-        for y in range(s.layers):
-            if self.tree:
-                G.gdn_tree_verify(self._dims1, self.n_nodes, self.parent_host, self.parent, self.x[:, y],
-                                  self.a[:, y], self.b[:, y], self.conv_w[y], self.ssm_state[:, y],
-                                  self.conv_state[:, y], self.ssm_ckpt[:, y], self.conv_ckpt[:, y],
-                                  self.out[:, y], self.dev_status, stream)
-            else:
-                G.gdn_verify_span(self._dims1, self.n_tok, self.x[:, y], self.a[:, y], self.b[:, y],
-                                  self.conv_w[y], self.ssm_state[:, y], self.conv_state[:, y],
-                                  self.ssm_ckpt[:, y], self.conv_ckpt[:, y], self.out[:, y],
-                                  self.dev_status, stream)
+        for y in range(self.shape.layers):
+            self.verify_block(0, 1, y, y + 1, "checkpoint", stream)
 
     def step_per_layer(self, stream=None):
         """verify (one launch per layer) -> accept -> restore (all layers)."""
@@ -201,6 +235,68 @@ class SpecStep:
         """One captured step on the current stream (capture() first)."""
         self._graph.replay()
 
+    def capture_host_step(self, host: dict, out_host: dict, commit: str = "checkpoint", chunks: int = 4):
+        """Capture the end-to-end step for fixed pinned host buffers (see
+        run_host_step) into one CUDA graph that pipelines the host link with
+        the verify:
+        - a copy branch DMAs x, a, b in `chunks` contiguous blocks in item
+          order (blocks(): layer ranges for one request, request ranges
+          otherwise), then logits, tokens (and parent);
+        - the verify of each block is its own launch on its own branch, and
+          starts as soon as its block has landed (the blocks' layers and
+          requests are independent), so only the first block's copy is
+          exposed;
+        - all branches join before the acceptance; then come the commit
+          (restore or replay) and the D2H copies of the result.
+        One eager host step runs first, outside the capture."""
+        finish = {"checkpoint": self.restore, "replay": self.commit_replay, "wy": self.commit_wy}[commit]
+        saved = getattr(self, "commit", "checkpoint")
+        self.commit = commit
+        run_host_step(self, host, out_host)
+        self.commit = saved
+        torch.cuda.synchronize(self.device)
+        blocks = self.blocks(chunks)
+        g = torch.cuda.CUDAGraph()
+        main = torch.cuda.Stream(device=self.device)
+        copy = torch.cuda.Stream(device=self.device)
+        branches = [torch.cuda.Stream(device=self.device) for _ in blocks]
+        main.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.graph(g, stream=main):
+            fork = torch.cuda.Event()
+            fork.record(main)
+            copy.wait_event(fork)
+            landed = []
+            with torch.cuda.stream(copy):
+                for b0, b1, y0, y1 in blocks:
+                    for name in ("x", "a", "b"):
+                        getattr(self, name)[b0:b1, y0:y1].copy_(host[name][b0:b1, y0:y1], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(copy)
+                    landed.append(e)
+                for name in ("logits", "tokens", "parent"):
+                    if name in host:
+                        getattr(self, name).copy_(host[name], non_blocking=True)
+            copied = torch.cuda.Event()
+            copied.record(copy)
+            done = []
+            for (b0, b1, y0, y1), e, br in zip(blocks, landed, branches):
+                br.wait_event(e)
+                self.verify_block(b0, b1, y0, y1, commit, stream=br)
+                d = torch.cuda.Event()
+                d.record(br)
+                done.append(d)
+            for d in done:
+                main.wait_event(d)
+            main.wait_event(copied)
+            self.accept(stream=main)
+            finish(stream=main)
+            for name in ("accept_len", "accept_node", "argmax"):
+                out_host[name].copy_(getattr(self, name), non_blocking=True)
+        torch.cuda.current_stream(self.device).wait_stream(main)
+        self._graph_host = g
+        self._graph_host_bufs = (host, out_host)
+        return g
+
     # -- algorithmic bytes -------------------------------------------------
     def verify_bytes(self) -> int:
         """Bytes the verify must move: S and conv state read once, every
@@ -254,21 +350,26 @@ def pinned_host_inputs(wl: Workload):
 
 def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None, graph: bool = False):
     """End-to-end step through the public API: H2D copy of the step's inputs
-    from pinned memory, verify -> accept -> restore (eagerly, or as the
-    captured graph), D2H copy of the result (accept_len, accept_node,
-    argmax). Returns (h2d_bytes, d2h_bytes)."""
-    h2d = 0
+    from pinned memory, verify -> accept -> commit, D2H copy of the result
+    (accept_len, accept_node, argmax). With graph=True the step is one graph
+    launch: the whole host step captured by capture_host_step for these
+    buffers, else the captured device step between eager copies. Returns
+    (h2d_bytes, d2h_bytes)."""
+    h2d = sum(host[n].numel() * host[n].element_size()
+              for n in ("x", "a", "b", "logits", "tokens", "parent") if n in host)
+    d2h = sum(out_host[n].numel() * out_host[n].element_size()
+              for n in ("accept_len", "accept_node", "argmax"))
+    bufs = getattr(st, "_graph_host_bufs", None)
+    if graph and bufs is not None and bufs[0] is host and bufs[1] is out_host:
+        st._graph_host.replay()
+        return h2d, d2h
     for name in ("x", "a", "b", "logits", "tokens", "parent"):
         if name in host:
-            dst = getattr(st, name)
-            dst.copy_(host[name], non_blocking=True)
-            h2d += host[name].numel() * host[name].element_size()
+            getattr(st, name).copy_(host[name], non_blocking=True)
     if graph:
         st.replay()
     else:
         st.step_fn(getattr(st, "commit", "checkpoint"))(stream)
-    d2h = 0
     for name in ("accept_len", "accept_node", "argmax"):
         out_host[name].copy_(getattr(st, name), non_blocking=True)
-        d2h += out_host[name].numel() * out_host[name].element_size()
     return h2d, d2h

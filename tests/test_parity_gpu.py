@@ -441,6 +441,39 @@ def test_host_buffer_step_matches_device_step():
     np.testing.assert_array_equal(out["argmax"][0].numpy(), am)
 
 
+@pytest.mark.parametrize("wid,commit", [(2, "checkpoint"), (3, "checkpoint"), (2, "replay"), (2, "wy")])
+def test_host_step_graph_equals_eager_host_steps(wid, commit):
+    """The whole host step as one graph (copies on two branches, the step,
+    the read-back) gives the eager host step's bytes, step after step."""
+    from speculative_decode_hybrid_gb300.pipeline import pinned_host_inputs, run_host_step
+    wl = W.make_workload(wid, seed=9, layers=2)
+    N = wl.shape.n_nodes
+    host = pinned_host_inputs(wl)
+
+    def outs():
+        return {"accept_len": torch.empty(1, dtype=torch.int32).pin_memory(),
+                "accept_node": torch.empty(1, dtype=torch.int32).pin_memory(),
+                "argmax": torch.empty((1, N), dtype=torch.int32).pin_memory()}
+
+    eager, graph = SpecStep(wl), SpecStep(wl)
+    eager.commit = commit
+    out_e, out_g = outs(), outs()
+    for _ in range(3):  # the capture runs one eager host step first
+        run_host_step(eager, host, out_e)
+    graph.capture_host_step(host, out_g, commit)
+    graph.x.zero_()  # the graph must copy the inputs in itself
+    graph.logits.zero_()
+    for _ in range(2):
+        run_host_step(graph, host, out_g, graph=True)
+    torch.cuda.synchronize()
+    for name in ("accept_len", "accept_node", "argmax"):
+        assert torch.equal(out_e[name], out_g[name]), name
+    for name in ("out", "ssm_state", "conv_state"):
+        assert torch.equal(getattr(eager, name), getattr(graph, name)), name
+    am, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0], wl.parent[0] if wl.parent is not None else None)
+    assert (int(out_g["accept_len"][0]), int(out_g["accept_node"][0])) == (kl, kn)
+
+
 # ------------------------------------------------------------ replay-commit variant
 
 def test_verify_without_checkpoints_matches_and_writes_none():
