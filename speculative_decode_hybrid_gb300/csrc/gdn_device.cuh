@@ -7,6 +7,34 @@
 
 namespace gdndev {
 
+// Programmatic dependent launch. pdl_wait(): wait until the kernels this
+// grid depends on (the previous work on the stream) have completed and their
+// writes are visible; returns at once for a grid launched without the
+// attribute. Every kernel of this library calls it before its first global
+// memory access. pdl_launch_dependents(): let the grid launched after this
+// one be scheduled now (it still waits for this grid's completion).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kern` with programmatic stream serialization, so that its launch
+// and scheduling overlap the tail of the previous kernel on the stream
+// (which pdl_wait() in `kern` then waits for).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Load element i of an input array stored as bf16 or f32, widened to f32
 // (bf16 -> f32 is exact).
 template <bool BF16>

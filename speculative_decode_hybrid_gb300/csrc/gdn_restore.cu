@@ -17,6 +17,9 @@
 
 namespace {
 
+using gdndev::launch_pdl;
+using gdndev::pdl_wait;
+
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 constexpr int kCtasPerSm = 8;
@@ -42,6 +45,7 @@ gdn_restore_kernel(int Y, int T, size_t ssm_slot, size_t conv_slot, const int32_
                    float *__restrict__ ssm_state, float *__restrict__ conv_state, int32_t *dev_status) {
     const int by = blockIdx.y;
     const int b = by / Y;
+    pdl_wait();  // accept_node and the checkpoints come from the kernels before
     const int node = accept_node[b];
     if (node == 0) return;
     if (node < 0 || node > T) {
@@ -96,8 +100,9 @@ extern "C" int gdn_rollback_restore(const gdn_dims *d, int32_t n_tok, const int3
     if ((size_t)chunks > max_chunks) chunks = (int)max_chunks;
     if (chunks < 1) chunks = 1;
     dim3 grid(chunks, rows);
-    gdn_restore_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        d->layers, n_tok, ssm_slot, conv_slot, accept_node_dev, ssm_ckpt, conv_ckpt, ssm_state, conv_state,
-        dev_status);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return launch_pdl(gdn_restore_kernel, grid, dim3(kThreads), 0, static_cast<cudaStream_t>(stream), d->layers,
+                      n_tok, ssm_slot, conv_slot, accept_node_dev, ssm_ckpt, conv_ckpt, ssm_state, conv_state,
+                      dev_status) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
 }

@@ -181,6 +181,7 @@ __device__ __forceinline__ void write_out(const VerifyArgs &p, const Item &I, co
 // ---------------------------------------------------------------------------
 template <int DK, bool BF16, bool TREE>
 __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArgs p) {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     const Layout L = make_layout(p.T, DK, p.K);
     float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     if (tid == 0) steal_init(bar);
     int it = blockIdx.x;
     if (it >= n_items) return;
+    pdl_wait();
     float ga = 0.f, gb = 0.f;
     int pr = 0;
     int tables_of = -1;  // request whose tree tables are in shared memory
@@ -392,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         __syncthreads();  // staging consumed; q, k, v ready; next_s set
 
         const int next = next_s >= 0 && next_s < n_items ? next_s : n_items;
+        if (next >= n_items) pdl_launch_dependents();  // nothing left to take: this CTA's last item
         bool next_reuse = false;
         if (next < n_items) {
             const Item In = decode_item(p, next, nrb);
@@ -423,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
 // conv window comes from the (not yet updated) live conv state.
 template <int DK, bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArgs p, const int32_t *accept_len) {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     const Layout L = make_layout(p.T, DK, p.K);
     float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
@@ -527,14 +531,15 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
         while (pa.rpi > kRowsPerWarp && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
         // one CTA per item: the running CTAs take the pending ones' items
         const int grid = batch * a.Y * a.H_v * row_blocks(pa);
-        kern<<<grid, threads, Lp.total, stream>>>(pa, grid);
+        if (launch_pdl(kern, dim3(grid), dim3(threads), Lp.total, stream, pa, grid) != cudaSuccess)
+            return GDN_ERR_CUDA;
     } else {
         auto kern = gdn_verify_kernel<DK, BF16, TREE>;
         static std::atomic<size_t> set{48 * 1024};
         const Layout L = make_layout(a.T, DK, a.K);
         if (!ensure_smem(kern, L.total, set)) return GDN_ERR_CUDA;
         dim3 grid(nrb, a.H_v, batch * a.Y);
-        kern<<<grid, threads, L.total, stream>>>(a);
+        if (launch_pdl(kern, grid, dim3(threads), L.total, stream, a) != cudaSuccess) return GDN_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -653,18 +658,21 @@ extern "C" int gdn_commit_replay(const gdn_dims *d, int32_t n_tok, const int32_t
         auto kern = bf ? gdn_replay_kernel<128, true> : gdn_replay_kernel<128, false>;
         static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
         if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
-        kern<<<grid, threads, L.total, st>>>(v, accept_len_dev);
+        if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
+            return GDN_ERR_CUDA;
     } else {
         auto kern = bf ? gdn_replay_kernel<64, true> : gdn_replay_kernel<64, false>;
         static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
         if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
-        kern<<<grid, threads, L.total, st>>>(v, accept_len_dev);
+        if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
+            return GDN_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     if (d->conv_k > 1) {
         const dim3 g2((d->conv_ch + 255) / 256, d->batch * d->layers);
-        if (bf) gdn_conv_state_kernel<true><<<g2, 256, 0, st>>>(v, accept_len_dev, conv_state);
-        else gdn_conv_state_kernel<false><<<g2, 256, 0, st>>>(v, accept_len_dev, conv_state);
+        if (launch_pdl(bf ? gdn_conv_state_kernel<true> : gdn_conv_state_kernel<false>, g2, dim3(256), 0, st, v,
+                       accept_len_dev, conv_state) != cudaSuccess)
+            return GDN_ERR_CUDA;
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
     return GDN_OK;

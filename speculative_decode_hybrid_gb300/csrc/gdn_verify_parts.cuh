@@ -499,6 +499,7 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
 template <bool BF16>
 __global__ void __launch_bounds__(256) gdn_conv_state_kernel(const VerifyArgs p, const int32_t *accept_len,
                                                             float *conv_state) {
+    pdl_wait();
     const int by = blockIdx.y, bidx = by / p.Y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     const int K = p.K, T = p.T;

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     const int nrb = row_blocks(p);
     const Item I = decode_item(p, blockIdx.x, nrb);
     const int tid = threadIdx.x, nthreads = blockDim.x;
+    pdl_wait();
 
     int Te = T;  // tokens that count: all for the verify, the accepted k for the commit
     if constexpr (COMMIT) {
@@ -339,8 +340,9 @@ int launch_wy(const VerifyArgs &a, int batch, const int32_t *accept_len, cudaStr
     auto kern = a.K == 4 ? gdn_wy_kernel<DK, BF16, 4, COMMIT> : gdn_wy_kernel<DK, BF16, 0, COMMIT>;
     static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
     if (!ensure_smem(kern, L.total, a.K == 4 ? set4 : set0)) return GDN_ERR_CUDA;
-    kern<<<(unsigned)n_items, kThreads, L.total, st>>>(a, accept_len);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return launch_pdl(kern, dim3((unsigned)n_items), dim3(kThreads), L.total, st, a, accept_len) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
 }
 
 template <bool COMMIT>
@@ -401,9 +403,9 @@ extern "C" int gdn_commit_wy(const gdn_dims *d, int32_t n_tok, const int32_t *ac
     if (rc != GDN_OK) return rc;
     if (d->conv_k > 1) {  // after the state kernel, which reads the old conv state
         const dim3 g2((d->conv_ch + 255) / 256, d->batch * d->layers);
-        if (d->in_dtype == GDN_BF16) gdn_conv_state_kernel<true><<<g2, 256, 0, st>>>(v, accept_len_dev, conv_state);
-        else gdn_conv_state_kernel<false><<<g2, 256, 0, st>>>(v, accept_len_dev, conv_state);
-        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+        if (launch_pdl(d->in_dtype == GDN_BF16 ? gdn_conv_state_kernel<true> : gdn_conv_state_kernel<false>, g2,
+                       dim3(256), 0, st, v, accept_len_dev, conv_state) != cudaSuccess)
+            return GDN_ERR_CUDA;
     }
     return GDN_OK;
 }

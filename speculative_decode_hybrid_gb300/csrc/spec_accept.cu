@@ -58,6 +58,8 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
 
     const int split = blockIdx.x, n = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
+    gdndev::pdl_wait();
+    gdndev::pdl_launch_dependents();  // the restore may be scheduled; it waits for this grid
     // the request's draft tokens / parents, loaded now so that the last CTA
     // does not wait for them after the ticket
     const int my_tok = tid < N ? tokens[(size_t)b * N + tid] : 0;
@@ -205,10 +207,11 @@ extern "C" int spec_accept_greedy(int32_t batch, int32_t n_nodes, int32_t vocab,
     unsigned long long *keys =
         reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + kCounterBytes(batch));
     dim3 grid(splits, n_nodes, batch);
-    spec_accept_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        n_nodes, vocab, splits, chunk, logits, tokens, parent_dev, argmax_out, accept_len, accept_node,
-        counters, keys, dev_status);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return gdndev::launch_pdl(spec_accept_kernel, grid, dim3(kThreads), 0, static_cast<cudaStream_t>(stream), n_nodes,
+                              vocab, splits, chunk, logits, tokens, parent_dev, argmax_out, accept_len, accept_node,
+                              counters, keys, dev_status) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------

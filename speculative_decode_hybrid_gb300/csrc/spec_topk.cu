@@ -58,6 +58,7 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *r = logits + (size_t)row * V;
     const int lo = split * chunk, hi = min(V, lo + chunk);
+    gdndev::pdl_wait();
 
     unsigned long long list = 0ull;
     if ((V & 3) == 0) {
