@@ -52,23 +52,26 @@
 namespace {
 
 
-// The register-resident state of this thread's rows (4 slots x NV4 float4).
-template <int DK>
+// The register-resident state of this thread's rows (SL slots x NV4 float4;
+// a warp holds 4 * SL rows). SL = 4 (16 rows per warp) is the default; small
+// launches use SL = 1 so that a head's few rows spread over more warps.
+template <int DK, int SL = kSlots>
 struct RowState {
     static constexpr int NV4 = DK / (4 * kLanesPerRow);
-    float4 S[kSlots][NV4];
-    int lrow[kSlots];
+    static constexpr int kRows = kRowsPerSlot * SL;  // rows per warp
+    float4 S[SL][NV4];
+    int lrow[SL];
 };
 
-template <int DK>
-__device__ __forceinline__ void load_rows(RowState<DK> &rs, const float *src, bool has_rows) {
+template <int DK, int SL>
+__device__ __forceinline__ void load_rows(RowState<DK, SL> &rs, const float *src, bool has_rows) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j8 = lane & (kLanesPerRow - 1), rsub = lane / kLanesPerRow;
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-        rs.lrow[s] = warp * kRowsPerWarp + s * kRowsPerSlot + rsub;
+    for (int s = 0; s < SL; ++s) {
+        rs.lrow[s] = warp * RowState<DK, SL>::kRows + s * kRowsPerSlot + rsub;
 #pragma unroll
-        for (int m = 0; m < RowState<DK>::NV4; ++m)
+        for (int m = 0; m < RowState<DK, SL>::NV4; ++m)
             rs.S[s][m] = has_rows ? ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -77,13 +80,13 @@ __device__ __forceinline__ void load_rows(RowState<DK> &rs, const float *src, bo
 // One node t of the recurrence for this thread's rows: one checkpoint slot.
 // s_in: the item's initial rows; ck0: slot 0 of the item's rows.
 // `prev` is the node whose state the registers hold (0: the initial state).
-template <int DK, bool TREE>
-__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK> &rs, int t, int prev,
+template <int DK, bool TREE, int SL>
+__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK, SL> &rs, int t, int prev,
                                                const float *s_in, float *ck0, const float *q_s,
                                                const float *k_s, const float *v_s, float *o_s,
                                                const float *a_s, const float *b_s, const float *kq_s,
                                                const int *par_s) {
-    constexpr int NV4 = RowState<DK>::NV4;
+    constexpr int NV4 = RowState<DK, SL>::NV4;
     const int lane = threadIdx.x & 31;
     const int j8 = lane & (kLanesPerRow - 1);
     const size_t slot = (size_t)p.H_v * p.d_v * DK;
@@ -92,7 +95,7 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
         if (pp != prev) {
             const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
 #pragma unroll
-            for (int s = 0; s < kSlots; ++s)
+            for (int s = 0; s < SL; ++s)
 #pragma unroll
                 for (int m = 0; m < NV4; ++m)
                     rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
@@ -105,9 +108,9 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
         qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
     }
     const float at = a_s[t], bt = b_s[t], kqt = kq_s[t];
-    float u[kSlots], w[kSlots];
+    float u[SL], w[SL];
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < SL; ++s) {
         u[s] = 0.f;
         w[s] = 0.f;
 #pragma unroll
@@ -119,14 +122,14 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
 #pragma unroll
     for (int off = 1; off < kLanesPerRow; off <<= 1) {
 #pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < SL; ++s) {
             u[s] += __shfl_xor_sync(0xffffffffu, u[s], off);
             w[s] += __shfl_xor_sync(0xffffffffu, w[s], off);
         }
     }
     float *ck = ck0 + (size_t)t * slot;
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < SL; ++s) {
         const float vv = v_s[(size_t)t * kRowsPerCta + rs.lrow[s]];
         const float c = bt * (vv - at * u[s]);
 #pragma unroll
@@ -144,8 +147,8 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
 }
 
 // The recurrence over all nodes of one item.
-template <int DK, bool TREE>
-__device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK> &rs, const float *s_in,
+template <int DK, bool TREE, int SL>
+__device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL> &rs, const float *s_in,
                                           float *ck0, const float *q_s, const float *k_s,
                                           const float *v_s, float *o_s, const float *a_s,
                                           const float *b_s, const float *kq_s, const int *par_s) {
@@ -154,12 +157,13 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK> &rs
         int prev = 0;
         for (int q = 0; q < p.T; ++q) {
             const int node = ord_s[q];
-            recurrence_step<DK, TREE>(p, rs, node - 1, prev, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+            recurrence_step<DK, TREE, SL>(p, rs, node - 1, prev, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
+                                          par_s);
             prev = node;
         }
     } else {
         for (int t = 0; t < p.T; ++t)
-            recurrence_step<DK, TREE>(p, rs, t, t, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+            recurrence_step<DK, TREE, SL>(p, rs, t, t, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
     }
 }
 
@@ -323,7 +327,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
 //
 // KT: the conv width as a compile-time constant (4 for Qwen3.5/3.6), or 0 to
 // read it from the arguments.
-template <int DK, bool BF16, bool TREE, int KT>
+//
+// SL: slots of 4 rows per warp in the recurrence (4 by default, 1 for small
+// launches, whose items have few rows).
+template <int DK, bool BF16, bool TREE, int KT, int SL>
 __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const VerifyArgs p, int n_items) {
     constexpr int ES = BF16 ? 2 : 4;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -361,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     while (true) {
         if (tid == 0 && stealing) steal_issue(resp, bar);  // the next item, answered during this prologue
         const Item I = decode_item(p, it, nrb);
-        const bool has_rows = warp * kRowsPerWarp < I.R;
+        const bool has_rows = warp * RowState<DK, SL>::kRows < I.R;
         const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-        RowState<DK> rs;
-        load_rows<DK>(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
+        RowState<DK, SL> rs;
+        load_rows(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
 
         cp_async_wait_all();
         if (tid < T) {
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         if (has_rows) {
             float *ck0 =
                 p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-            recurrence<DK, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+            recurrence<DK, TREE, SL>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
         }
         __syncthreads();
         write_out(p, I, o_s, threadIdx.x, blockDim.x);
@@ -516,22 +523,33 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     const PipeLayout Lp = make_pipe_layout(a.T, DK, a.K, BF16 ? 2 : 4);
     // the persistent kernel keeps one gate / parent value per thread in registers
     if (aligned_inputs && Lp.total + kStaticSmem <= kMaxSmem && threads > a.T) {
-        auto kern = a.K == 4 ? gdn_verify_persistent<DK, BF16, TREE, 4> : gdn_verify_persistent<DK, BF16, TREE, 0>;
-        static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
-        std::atomic<size_t> &set = a.K == 4 ? set4 : set0;
-        if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
         // Small launches (one layer, a few heads) split each head's rows into
-        // smaller blocks until there are items for about two resident CTAs
-        // per SM; every CTA still runs its item's whole conv prologue, and
-        // only the warps that own rows run the recurrence. Each row's
-        // arithmetic is the same whatever the block size.
+        // smaller blocks, down to 32 rows, until there are items for about
+        // two resident CTAs per SM; every CTA still runs its item's whole
+        // conv prologue. Items of <= 32 rows run the recurrence with 4 rows
+        // per warp (SL = 1), so that all the CTA's warps share them. (A
+        // layer as 128 CTAs of 32 rows ran 48 back-to-back launches in 675
+        // us, as 256 CTAs of 16 rows in 880 us, as 32 CTAs of 128 rows in
+        // 773 us.) Each row's arithmetic is the same whatever the block size
+        // or the warp that holds it. Without the K = 4 instantiation, blocks
+        // go down to 16 rows with 16 rows per warp.
         VerifyArgs pa = a;
         const int sms = gdnhost::sm_count();
         const long long want = 2LL * (sms > 0 ? sms : 152);
-        while (pa.rpi > kRowsPerWarp && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
+        const int min_rpi = a.K == 4 ? 32 : kRowsPerWarp;
+        while (pa.rpi > min_rpi && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
+        const bool small = pa.rpi <= 32 && a.K == 4;
+        // with 4 rows per warp an item of rpi rows needs rpi / 4 warps
+        const int thr = small && threads < pa.rpi / kRowsPerSlot * 32 ? pa.rpi / kRowsPerSlot * 32 : threads;
+        auto kern = small ? gdn_verify_persistent<DK, BF16, TREE, 4, 1>
+                          : (a.K == 4 ? gdn_verify_persistent<DK, BF16, TREE, 4, kSlots>
+                                      : gdn_verify_persistent<DK, BF16, TREE, 0, kSlots>);
+        static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024}, set1{48 * 1024};
+        std::atomic<size_t> &set = small ? set1 : (a.K == 4 ? set4 : set0);
+        if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
         // one CTA per item: the running CTAs take the pending ones' items
         const int grid = batch * a.Y * a.H_v * row_blocks(pa);
-        if (launch_pdl(kern, dim3(grid), dim3(threads), Lp.total, stream, pa, grid) != cudaSuccess)
+        if (launch_pdl(kern, dim3(grid), dim3(thr), Lp.total, stream, pa, grid) != cudaSuccess)
             return GDN_ERR_CUDA;
     } else {
         auto kern = gdn_verify_kernel<DK, BF16, TREE>;
