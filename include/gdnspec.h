@@ -87,9 +87,9 @@ typedef void *gdn_stream_t;
 #define GDN_DEV_TREE 0x8          /* a device parent array broke parent[i] in [0, i): the kernel
                                      used parent i-1 for that node (verify) or left it unmatched
                                      (acceptance) instead of reading out of bounds */
-#define GDN_DEV_SCHED 0x10        /* verify: a CTA gave up waiting for the hardware's answer to
-                                     a work-stealing request; the item it may have been given
-                                     was not computed (outputs incomplete) */
+#define GDN_DEV_SCHED 0x10        /* verify: a CTA gave up waiting for an asynchronous hardware
+                                     operation (the answer to a work-stealing request, or a
+                                     tensor-core product); its outputs are incomplete */
 
 /* Limits of this library. */
 #define GDN_MAX_TOKENS 64         /* n_tok (= N - 1) per span */

@@ -25,17 +25,21 @@
 // state (the staged prologue of the verify kernel) and the head's 128 x d_k
 // state rows into shared memory. The state tile and the [K | Q] tile are
 // kept in the 128-byte-swizzled K-major layout of the tensor-core operand
-// descriptors. Thread r < 128 owns state row r: it forms g and h against
-// the [K | Q] tile (broadcast reads), runs the forward substitution in
-// registers and writes o_t for every t (consecutive threads, consecutive
-// addresses). The products over d_k (S_0 [K | Q]; for the commit S_0 K and
-// the update A S_0 + C K) are register-blocked over all 256 threads.
+// descriptors.
+//  * Verify: S_0 [K | Q] (M = 128 rows, N = 2T <= 32, K = d_k) runs on the
+//    5th-generation tensor cores (tcgen05.mma kind::tf32, accumulator in
+//    tensor memory) as 3 x TF32, which keeps f32 accuracy; thread r < 128
+//    reads row r of the accumulator (tcgen05.ld), runs the forward
+//    substitution in registers and writes o_t for every t.
+//  * Commit: S_0 K over the k accepted tokens and the update A S_0 + C K
+//    are register-blocked over all 256 threads on the FMA pipe.
 #include <cuda_runtime.h>
 
 #include <atomic>
 
 #include "gdn_device.cuh"
 #include "gdn_host.h"
+#include "gdn_tc.cuh"
 #include "gdn_verify_parts.cuh"
 #include "gdnspec.h"
 
@@ -44,6 +48,11 @@ namespace {
 constexpr int kWyMaxT = GDN_WY_MAX_TOKENS;  // tokens per span in this form
 constexpr int kWyRows = kRowsPerCta;  // value rows per item (128)
 constexpr int kWyB = 2 * kWyMaxT;     // rows of the [K | Q] tile
+// tensor memory of the verify's product: the small part of S_0 (d_k <= 128
+// columns) and the accumulator (kWyB columns from column 128)
+constexpr int kWyTmemCols = 256;
+constexpr unsigned kWyTmemD = 128;
+constexpr unsigned kWyPolls = 1u << 22;  // bound on the wait for the product
 
 // Byte offset of the 16-byte unit ug of row r in a K-major tile of `rows`
 // rows whose row is split in 128-byte chunks: chunk-major, then row, the
@@ -58,7 +67,7 @@ __host__ __device__ __forceinline__ unsigned swz(int rows, int r, int ug) {
 // aligned offset), then the staging buffers, which the [K | Q] tile reuses
 // once the prologue has consumed them, then the small arrays.
 struct WyLayout {
-    size_t s0, xst, wst, cst, bkq, q, k, v, a, b, kq, ac, lm, mm, dm, total;
+    size_t s0, xst, wst, cst, bkq, q, k, v, a, b, kq, ac, lm, mm, dm, bar, tmem, total;
 };
 
 __host__ __device__ inline WyLayout make_wy_layout(int T, int DK, int K, int esize) {
@@ -76,13 +85,18 @@ __host__ __device__ inline WyLayout make_wy_layout(int T, int DK, int K, int esi
     L.bkq = off;
     const size_t bkq_end = off + (size_t)kWyB * DK * 4;
     off = o2 > bkq_end ? o2 : bkq_end;
-    // q and k; once the small matrices are formed the commit keeps its
-    // G / coefficient rows (kWyRows x (kWyMaxT + 1) floats at most) here
+    // q and k. Once the small matrices are formed the region is reused: by
+    // the verify's tensor-core product for the small part of [K | Q] (a
+    // kWyB-row swizzled tile, 1024-byte aligned), by the commit for its G /
+    // coefficient rows (kWyRows x (kWyMaxT + 1) floats at most).
+    off = (off + 1023) & ~size_t(1023);
     L.q = off;
     L.k = al16(off + (size_t)T * DK * 4);
     {
-        const size_t qk_end = L.k + (size_t)T * DK * 4, g_end = L.q + (size_t)kWyRows * (kWyMaxT + 1) * 4;
-        off = al16(qk_end > g_end ? qk_end : g_end);
+        size_t end = L.k + (size_t)T * DK * 4;
+        const size_t g_end = L.q + (size_t)kWyRows * (kWyMaxT + 1) * 4, b_end = L.q + (size_t)kWyB * DK * 4;
+        end = end > g_end ? end : g_end;
+        off = al16(end > b_end ? end : b_end);
     }
     L.v = off; off = al16(off + (size_t)T * kWyRows * 4);
     L.a = off; off = al16(off + (size_t)T * 4);
@@ -92,6 +106,8 @@ __host__ __device__ inline WyLayout make_wy_layout(int T, int DK, int K, int esi
     L.lm = off; off = al16(off + (size_t)T * T * 4);
     L.mm = off; off = al16(off + (size_t)T * T * 4);
     L.dm = off; off = al16(off + (size_t)T * T * 4);
+    L.bar = off; off += 8;   // mbarrier of the tensor-core product
+    L.tmem = off; off += 8;  // tensor-memory base address
     L.total = off;
     return L;
 }
@@ -103,9 +119,23 @@ template <int DK, bool BF16, int KT, bool COMMIT>
 __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p, const int32_t *accept_len) {
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int U = DK / 4;  // 16-byte units per state row
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
     const int T = p.T, K = KT > 0 ? KT : p.K;
     const WyLayout L = make_wy_layout(T, DK, K, ES);
+    // The verify's S_0 [K | Q] product runs on the tensor cores when the
+    // shared tiles sit on the 1024-byte boundary the hardware swizzle
+    // assumes; otherwise (never seen) on the FMA pipe with the same swizzle.
+    const unsigned smem_base = (unsigned)__cvta_generic_to_shared(smem);
+    const bool tc = !COMMIT && (smem_base & 1023u) == 0;
+    unsigned *tmem_s = reinterpret_cast<unsigned *>(smem + L.tmem);
+    const unsigned bar = smem_base + (unsigned)L.bar;
+    if (tc) {
+        if (threadIdx.x < 32) gdntc::tmem_alloc<kWyTmemCols>(tmem_s);
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+            gdntc::fence_smem_to_async();
+        }
+    }
     unsigned char *s0 = smem + L.s0, *bkq = smem + L.bkq;
     unsigned char *xst = smem + L.xst, *wst = smem + L.wst, *cst = smem + L.cst;
     float *q_s = reinterpret_cast<float *>(smem + L.q), *k_s = reinterpret_cast<float *>(smem + L.k);
@@ -213,7 +243,94 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     const int gs = NV | 1;
     float *gh = COMMIT ? q_s : reinterpret_cast<float *>(s0);
     static_assert(kWyRows * (kWyB + 1) * 4 <= kWyRows * 64 * 4, "the verify's G fits in the state tile");
-    {
+    if (tc) {
+        // Tensor cores, kind::tf32 at f32 accuracy (3 x TF32): with
+        // x = big + small, big = tf32(x), the product is
+        // big(S_0) big(B) + big(S_0) small(B) + small(S_0) big(B) (the
+        // small x small term is below f32 rounding). big(S_0) replaces the
+        // state tile in place and small(S_0) goes to tensor memory (thread
+        // r < 128 owns row r, its warp's 32 lanes); big(B) replaces the
+        // [K | Q] tile, small(B) goes over the dead q / k. Rows of the
+        // tiles beyond R / 2T hold stale bytes and only feed dropped
+        // accumulator rows / columns.
+        gdntc::fence_before_sync();
+        __syncthreads();  // the tensor-memory address is visible
+        gdntc::fence_after_sync();
+        const unsigned tmem = *tmem_s;
+        unsigned char *bsm = reinterpret_cast<unsigned char *>(q_s);
+        if (tid < kWyRows) {
+            const unsigned lanes = tmem + ((unsigned)(tid & ~31) << 16);
+#pragma unroll 1
+            for (int c0 = 0; c0 < DK; c0 += 8) {
+                unsigned v[8];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float4 *pp = reinterpret_cast<float4 *>(s0 + swz(kWyRows, tid, (c0 >> 2) + h2));
+                    const float4 x = *pp;
+                    const float4 hi = make_float4(gdntc::tf32_rna(x.x), gdntc::tf32_rna(x.y), gdntc::tf32_rna(x.z),
+                                                  gdntc::tf32_rna(x.w));
+                    *pp = hi;
+                    v[4 * h2 + 0] = __float_as_uint(x.x - hi.x);
+                    v[4 * h2 + 1] = __float_as_uint(x.y - hi.y);
+                    v[4 * h2 + 2] = __float_as_uint(x.z - hi.z);
+                    v[4 * h2 + 3] = __float_as_uint(x.w - hi.w);
+                }
+                gdntc::tmem_st8(lanes + (unsigned)c0, v);
+            }
+            gdntc::tmem_wait_st();
+        } else {
+            for (int i = tid - kWyRows; i < kWyB * U; i += nthreads - kWyRows) {
+                const int n = i / U, ug = i - n * U;
+                float4 *pp = reinterpret_cast<float4 *>(bkq + swz(kWyB, n, ug));
+                const float4 x = *pp;
+                const float4 hi = make_float4(gdntc::tf32_rna(x.x), gdntc::tf32_rna(x.y), gdntc::tf32_rna(x.z),
+                                              gdntc::tf32_rna(x.w));
+                *pp = hi;
+                *reinterpret_cast<float4 *>(bsm + swz(kWyB, n, ug)) =
+                    make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+            }
+        }
+        gdntc::fence_smem_to_async();
+        gdntc::fence_before_sync();
+        __syncthreads();
+        gdntc::fence_after_sync();
+        const unsigned tD = tmem + kWyTmemD;
+        if (tid == 0) {
+            constexpr unsigned idesc = gdntc::idesc_tf32(kWyRows, kWyB);
+            const unsigned a0 = smem_base + (unsigned)L.s0, b0 = smem_base + (unsigned)L.bkq,
+                           bs0 = smem_base + (unsigned)L.q;
+#pragma unroll 1
+            for (int ks = 0; ks < DK / 8; ++ks) {
+                const unsigned in_chunk = (unsigned)(ks & 3) * 32u;
+                const uint64_t da = gdntc::smem_desc_sw128(a0 + (unsigned)(ks >> 2) * (kWyRows * 128u) + in_chunk);
+                const uint64_t db = gdntc::smem_desc_sw128(b0 + (unsigned)(ks >> 2) * (kWyB * 128u) + in_chunk);
+                const uint64_t dbs = gdntc::smem_desc_sw128(bs0 + (unsigned)(ks >> 2) * (kWyB * 128u) + in_chunk);
+                gdntc::mma_tf32_ss(tD, da, db, idesc, ks > 0);
+                gdntc::mma_tf32_ss(tD, da, dbs, idesc, true);
+                gdntc::mma_tf32_ts(tD, tmem + (unsigned)ks * 8u, db, idesc, true);
+            }
+            gdntc::mma_commit(bar);
+        }
+        if (!gdntc::mbar_wait(bar, 0, kWyPolls)) {
+            if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GDN_DEV_SCHED);
+            gdntc::mbar_wait(bar, 0, kWyPolls);  // the product may still be running: wait once more
+        }
+        gdntc::fence_after_sync();
+        if (tid < kWyRows) {
+            unsigned v[32];
+            gdntc::tmem_ld32(tD + ((unsigned)(tid & ~31) << 16), v);
+            gdntc::tmem_wait_ld();
+            if (tid < I.R) {
+#pragma unroll
+                for (int n = 0; n < kWyB; ++n)
+                    if (n < NV) gh[tid * gs + n] = __uint_as_float(v[n]);
+            }
+        }
+        gdntc::fence_before_sync();
+        __syncthreads();  // G is in shared memory; the tensor memory is no longer read
+        gdntc::fence_after_sync();
+        if (tid < 32) gdntc::tmem_dealloc<kWyTmemCols>(tmem);
+    } else {
         float acc[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)

@@ -589,7 +589,10 @@ def test_wy_verify_vs_oracle(name):
         for y, (ck, cc, out) in enumerate(refs):
             e = slice_rel_err(out_wy[r, y].cpu().numpy(), out, s.d_v)
             assert e <= TOL, (name, r, y, e)
-            assert slice_rel_err(out_wy[r, y].cpu().numpy(), st.out[r, y].cpu().numpy(), s.d_v) <= TOL
+            # f32 accuracy in both forms (the tensor-core product runs as 3 x TF32:
+            # a single TF32 pass would be off by ~1e-3 relative)
+            e2 = slice_rel_err(out_wy[r, y].cpu().numpy(), st.out[r, y].cpu().numpy(), s.d_v)
+            assert e2 <= 1e-4, (name, r, y, e2)
     assert int(st.dev_status.item()) == 0
 
 
