@@ -517,7 +517,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
 template <int DK, bool BF16, bool TREE>
 int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStream_t stream) {
     const int nrb = row_blocks(a);
-    const int n_items = batch * a.Y * a.H_v * nrb;
     const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;  // d_v % kRowsPerWarp == 0
     const int threads = rows / kRowsPerWarp * 32;
     const PipeLayout Lp = make_pipe_layout(a.T, DK, a.K, BF16 ? 2 : 4);

@@ -108,7 +108,10 @@ __host__ __device__ inline WyLayout make_wy_layout(int T, int DK, int K, int esi
     L.dm = off; off = al16(off + (size_t)T * T * 4);
     L.bar = off; off += 8;   // mbarrier of the tensor-core product
     L.tmem = off; off += 8;  // tensor-memory base address
-    L.total = off;
+    // the offsets above are relative to the first 1024-byte boundary of the
+    // dynamic shared memory (the tensor-core swizzle's period): up to 1 KB
+    // of slack in front
+    L.total = off + 1024;
     return L;
 }
 
@@ -119,17 +122,20 @@ template <int DK, bool BF16, int KT, bool COMMIT>
 __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p, const int32_t *accept_len) {
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int U = DK / 4;  // 16-byte units per state row
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     const int T = p.T, K = KT > 0 ? KT : p.K;
     const WyLayout L = make_wy_layout(T, DK, K, ES);
-    // The verify's S_0 [K | Q] product runs on the tensor cores when the
-    // shared tiles sit on the 1024-byte boundary the hardware swizzle
-    // assumes; otherwise (never seen) on the FMA pipe with the same swizzle.
+    // The tiles start on a 1024-byte boundary, the period of the hardware's
+    // 128-byte swizzle, wherever the dynamic shared memory begins.
+    const unsigned raw_base = (unsigned)__cvta_generic_to_shared(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
     const unsigned smem_base = (unsigned)__cvta_generic_to_shared(smem);
-    const bool tc = !COMMIT && (smem_base & 1023u) == 0;
+    // The verify's S_0 [K | Q] product runs on the tensor cores; the
+    // commit's products on the FMA pipe.
+    constexpr bool tc = !COMMIT;
     unsigned *tmem_s = reinterpret_cast<unsigned *>(smem + L.tmem);
     const unsigned bar = smem_base + (unsigned)L.bar;
-    if (tc) {
+    if constexpr (tc) {
         if (threadIdx.x < 32) gdntc::tmem_alloc<kWyTmemCols>(tmem_s);
         if (threadIdx.x == 0) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     const int gs = NV | 1;
     float *gh = COMMIT ? q_s : reinterpret_cast<float *>(s0);
     static_assert(kWyRows * (kWyB + 1) * 4 <= kWyRows * 64 * 4, "the verify's G fits in the state tile");
-    if (tc) {
+    if constexpr (tc) {
         // Tensor cores, kind::tf32 at f32 accuracy (3 x TF32): with
         // x = big + small, big = tf32(x), the product is
         // big(S_0) big(B) + big(S_0) small(B) + small(S_0) big(B) (the
