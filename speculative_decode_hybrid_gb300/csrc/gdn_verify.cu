@@ -35,6 +35,12 @@
 //    compute; its state loads are issued first and overlap it.
 //    Items whose staging does not fit in shared memory (long f32 spans) use
 //    the one-item-per-CTA kernel, which loads its inputs directly.
+//  * Small launches (one layer at a time) split heads into blocks of down to
+//    32 rows and hold 4 rows per warp instead of 16, so that the GPU's SMs
+//    and each CTA's warps all get rows.
+//  * Kernels are launched with programmatic dependent launch: each waits
+//    (griddepcontrol.wait) for the previous kernel on the stream before its
+//    first global access, so its launch overlaps that kernel's tail.
 //  * Tree: nodes run in depth-first preorder (children in index order);
 //    when a node's parent is not the node just processed, each thread
 //    reloads its rows of the parent's checkpoint, which it wrote itself
@@ -520,7 +526,8 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;  // d_v % kRowsPerWarp == 0
     const int threads = rows / kRowsPerWarp * 32;
     const PipeLayout Lp = make_pipe_layout(a.T, DK, a.K, BF16 ? 2 : 4);
-    // the persistent kernel keeps one gate / parent value per thread in registers
+    // the work-stealing kernel (gdn_verify_persistent: its CTAs stay resident and take
+    // item after item) keeps one gate / parent value per thread in registers
     if (aligned_inputs && Lp.total + kStaticSmem <= kMaxSmem && threads > a.T) {
         // Small launches (one layer, a few heads) split each head's rows into
         // smaller blocks, down to 32 rows, until there are items for about

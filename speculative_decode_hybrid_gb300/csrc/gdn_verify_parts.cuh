@@ -341,7 +341,7 @@ __device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item
     if constexpr (TREE) pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I.bidx * (T + 1) + tid]) : 0;
 }
 
-// Shared-memory carve-up of the persistent kernel: the item's buffers plus
+// Shared-memory carve-up of the work-stealing kernel: the item's buffers plus
 // the staging of the next item's inputs.
 struct PipeLayout {
     size_t q, k, v, o, a, b, kq, par, src, xst, wst, cst, total;

@@ -232,17 +232,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     cp_async_wait_all();
     __syncthreads();  // state tile, [K | Q] tile and the small matrices are visible
 
-    // First product, register-blocked: G = S_0 [K | Q] (verify: 2T vectors)
-    // or G = S_0 K over the Te accepted tokens (commit). Thread (row group
-    // rg, column group cg) accumulates rows rg + 32 j against vectors
-    // cg + 8 i (j, i < 4): per 16-byte unit 8 shared loads for 64 FMAs. For
-    // one (j, i) the 8 row groups of a warp read 8 rows of distinct r mod 8
-    // (distinct bank groups under the swizzle) and its 4 column groups 4
-    // vectors of distinct n mod 8. Rows >= R read unused tile rows and are
-    // dropped. G goes through shared memory (rows padded to an odd stride)
-    // to the thread that owns the row: in the dead state tile for the
-    // verify, over the dead q / k for the commit (whose update still reads
-    // the state tile).
+    // First product: G = S_0 [K | Q] (verify: 2T vectors, tensor cores) or
+    // G = S_0 K over the Te accepted tokens (commit, FMA pipe). G goes
+    // through shared memory (rows padded to an odd stride) to the thread
+    // that owns the row: in the dead state tile for the verify, over the
+    // dead q / k for the commit (whose update still reads the state tile).
     const int warp = tid >> 5, lane = tid & 31;
     const int rg = (warp & 3) * 8 + (lane & 7), cg = (warp >> 2) * 4 + (lane >> 3);
     const int NV = COMMIT ? Te : 2 * T;
@@ -337,6 +331,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
         gdntc::fence_after_sync();
         if (tid < 32) gdntc::tmem_dealloc<kWyTmemCols>(tmem);
     } else {
+        // Register-blocked on the FMA pipe: thread (row group rg, column
+        // group cg) accumulates rows rg + 32 j against vectors cg + 8 i
+        // (j, i < 4), per 16-byte unit 8 shared loads for 64 FMAs. For one
+        // (j, i) the 8 row groups of a warp read 8 rows of distinct r mod 8
+        // (distinct bank groups under the swizzle) and its 4 column groups 4
+        // vectors of distinct n mod 8. Rows >= R read unused tile rows and
+        // are dropped.
         float acc[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
