@@ -116,6 +116,14 @@ __device__ __forceinline__ void tmem_st8(unsigned taddr, const unsigned (&v)[8])
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Warp-collective: 8 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(unsigned taddr, unsigned (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // Warp-collective: 32 consecutive 32-bit columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(unsigned taddr, unsigned (&v)[32]) {
     asm volatile(

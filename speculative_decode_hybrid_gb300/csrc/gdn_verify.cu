@@ -52,6 +52,7 @@
 
 #include "gdn_device.cuh"
 #include "gdn_host.h"
+#include "gdn_tc.cuh"
 #include "gdn_verify_parts.cuh"
 #include "gdnspec.h"
 
@@ -65,6 +66,7 @@ template <int DK, int SL = kSlots>
 struct RowState {
     static constexpr int NV4 = DK / (4 * kLanesPerRow);
     static constexpr int kRows = kRowsPerSlot * SL;  // rows per warp
+    static constexpr int kWords = SL * NV4 * 4;       // floats of state per thread
     float4 S[SL][NV4];
     int lrow[SL];
 };
@@ -83,15 +85,56 @@ __device__ __forceinline__ void load_rows(RowState<DK, SL> &rs, const float *src
     }
 }
 
+// Trees park each thread's initial rows in tensor memory (its own lane;
+// warps 4..7 use the columns after those of warps 0..3), so that the root's
+// later children restart from there instead of from DRAM. Warp-collective.
+template <int DK, int SL>
+__device__ __forceinline__ unsigned park_addr(unsigned tmem) {
+    const int warp = threadIdx.x >> 5;
+    return tmem + ((unsigned)(32 * (warp & 3)) << 16) + (unsigned)((warp >> 2) * RowState<DK, SL>::kWords);
+}
+
+template <int DK, int SL>
+__device__ __forceinline__ void park_rows(const RowState<DK, SL> &rs, unsigned tmem) {
+    constexpr int NV4 = RowState<DK, SL>::NV4;
+    static_assert((SL * NV4) % 2 == 0, "8 words per tensor-memory store");
+    const unsigned base = park_addr<DK, SL>(tmem);
+#pragma unroll
+    for (int k = 0; k < SL * NV4; k += 2) {
+        const float4 x = rs.S[k / NV4][k % NV4], y = rs.S[(k + 1) / NV4][(k + 1) % NV4];
+        const unsigned v[8] = {__float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w),
+                               __float_as_uint(y.x), __float_as_uint(y.y), __float_as_uint(y.z), __float_as_uint(y.w)};
+        gdntc::tmem_st8(base + (unsigned)(4 * k), v);
+    }
+    gdntc::tmem_wait_st();
+}
+
+template <int DK, int SL>
+__device__ __forceinline__ void fetch_rows(RowState<DK, SL> &rs, unsigned tmem) {
+    constexpr int NV4 = RowState<DK, SL>::NV4;
+    const unsigned base = park_addr<DK, SL>(tmem);
+#pragma unroll
+    for (int k = 0; k < SL * NV4; k += 2) {
+        unsigned v[8];
+        gdntc::tmem_ld8(base + (unsigned)(4 * k), v);
+        gdntc::tmem_wait_ld();
+        rs.S[k / NV4][k % NV4] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                             __uint_as_float(v[3]));
+        rs.S[(k + 1) / NV4][(k + 1) % NV4] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]),
+                                                         __uint_as_float(v[6]), __uint_as_float(v[7]));
+    }
+}
+
 // One node t of the recurrence for this thread's rows: one checkpoint slot.
 // s_in: the item's initial rows; ck0: slot 0 of the item's rows.
 // `prev` is the node whose state the registers hold (0: the initial state).
-template <int DK, bool TREE, int SL>
+// PARK: the initial rows are parked in tensor memory at `tmem` (trees).
+template <int DK, bool TREE, int SL, bool PARK = false>
 __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK, SL> &rs, int t, int prev,
                                                const float *s_in, float *ck0, const float *q_s,
                                                const float *k_s, const float *v_s, float *o_s,
                                                const float *a_s, const float *b_s, const float *kq_s,
-                                               const int *par_s) {
+                                               const int *par_s, unsigned tmem = 0) {
     constexpr int NV4 = RowState<DK, SL>::NV4;
     const int lane = threadIdx.x & 31;
     const int j8 = lane & (kLanesPerRow - 1);
@@ -99,12 +142,16 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
     if constexpr (TREE) {
         const int pp = par_s[t + 1];
         if (pp != prev) {
-            const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
+            if (PARK && pp == 0) {
+                fetch_rows(rs, tmem);
+            } else {
+                const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
 #pragma unroll
-            for (int s = 0; s < SL; ++s)
+                for (int s = 0; s < SL; ++s)
 #pragma unroll
-                for (int m = 0; m < NV4; ++m)
-                    rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
+                    for (int m = 0; m < NV4; ++m)
+                        rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
+            }
         }
     }
     float4 kk[NV4], qq[NV4];
@@ -153,18 +200,20 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
 }
 
 // The recurrence over all nodes of one item.
-template <int DK, bool TREE, int SL>
+template <int DK, bool TREE, int SL, bool PARK = false>
 __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL> &rs, const float *s_in,
                                           float *ck0, const float *q_s, const float *k_s,
                                           const float *v_s, float *o_s, const float *a_s,
-                                          const float *b_s, const float *kq_s, const int *par_s) {
+                                          const float *b_s, const float *kq_s, const int *par_s,
+                                          unsigned tmem = 0) {
     if constexpr (TREE) {
         const int *ord_s = par_s + (p.T + 1);  // depth-first order of the nodes
+        if constexpr (PARK) park_rows(rs, tmem);  // the loads issued at the item's start have landed by now
         int prev = 0;
         for (int q = 0; q < p.T; ++q) {
             const int node = ord_s[q];
-            recurrence_step<DK, TREE, SL>(p, rs, node - 1, prev, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
-                                          par_s);
+            recurrence_step<DK, TREE, SL, PARK>(p, rs, node - 1, prev, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s,
+                                                kq_s, par_s, tmem);
             prev = node;
         }
     } else {
@@ -354,6 +403,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     // work stealing: this CTA's own item first, then items of cancelled CTAs
     __shared__ __align__(16) unsigned long long steal_s[3];  // response (16 B), mbarrier
     __shared__ int next_s;
+    __shared__ unsigned park_s;  // tensor-memory columns of the parked initial rows (trees)
+    constexpr int kParkCols = 2 * RowState<DK, SL>::kWords <= 32    ? 32
+                              : 2 * RowState<DK, SL>::kWords <= 64  ? 64
+                              : 2 * RowState<DK, SL>::kWords <= 128 ? 128
+                                                                     : 256;
     const unsigned resp = (unsigned)__cvta_generic_to_shared(steal_s);
     const unsigned bar = resp + 16;
     unsigned phase = 0;
@@ -361,6 +415,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     if (tid == 0) steal_init(bar);
     int it = blockIdx.x;
     if (it >= n_items) return;
+    if constexpr (TREE) {
+        if (warp == 0) gdntc::tmem_alloc<kParkCols>(&park_s);
+        gdntc::fence_before_sync();
+        __syncthreads();
+        gdntc::fence_after_sync();
+    }
     pdl_wait();
     float ga = 0.f, gb = 0.f;
     int pr = 0;
@@ -420,13 +480,19 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         if (has_rows) {
             float *ck0 =
                 p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-            recurrence<DK, TREE, SL>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+            recurrence<DK, TREE, SL, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
+                                           par_s, TREE ? park_s : 0u);
         }
         __syncthreads();
         write_out(p, I, o_s, threadIdx.x, blockDim.x);
         if (next >= n_items) break;
         it = next;
         reuse_qk = next_reuse;
+    }
+    if constexpr (TREE) {
+        gdntc::fence_before_sync();
+        __syncthreads();  // no warp reads its parked rows any more
+        if (warp == 0) gdntc::tmem_dealloc<kParkCols>(park_s);
     }
 }
 
