@@ -404,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     __shared__ __align__(16) unsigned long long steal_s[3];  // response (16 B), mbarrier
     __shared__ int next_s;
     __shared__ unsigned park_s;  // tensor-memory columns of the parked initial rows (trees)
+    // Parking pays where an item's later root children would re-read its
+    // initial rows from DRAM: big launches. A small launch's checkpoints stay
+    // in L2, so the 4-rows-per-warp instantiation does not park.
+    constexpr bool kPark = TREE && SL == kSlots;
     constexpr int kParkCols = 2 * RowState<DK, SL>::kWords <= 32    ? 32
                               : 2 * RowState<DK, SL>::kWords <= 64  ? 64
                               : 2 * RowState<DK, SL>::kWords <= 128 ? 128
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     if (tid == 0) steal_init(bar);
     int it = blockIdx.x;
     if (it >= n_items) return;
-    if constexpr (TREE) {
+    if constexpr (kPark) {
         if (warp == 0) gdntc::tmem_alloc<kParkCols>(&park_s);
         gdntc::fence_before_sync();
         __syncthreads();
@@ -480,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         if (has_rows) {
             float *ck0 =
                 p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-            recurrence<DK, TREE, SL, TREE>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
-                                           par_s, TREE ? park_s : 0u);
+            recurrence<DK, TREE, SL, kPark>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
+                                            par_s, kPark ? park_s : 0u);
         }
         __syncthreads();
         write_out(p, I, o_s, threadIdx.x, blockDim.x);
@@ -489,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         it = next;
         reuse_qk = next_reuse;
     }
-    if constexpr (TREE) {
+    if constexpr (kPark) {
         gdntc::fence_before_sync();
         __syncthreads();  // no warp reads its parked rows any more
         if (warp == 0) gdntc::tmem_dealloc<kParkCols>(park_s);
