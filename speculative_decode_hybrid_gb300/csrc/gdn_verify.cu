@@ -41,11 +41,13 @@
 //  * Kernels are launched with programmatic dependent launch: each waits
 //    (griddepcontrol.wait) for the previous kernel on the stream before its
 //    first global access, so its launch overlaps that kernel's tail.
-//  * Tree: nodes run in depth-first preorder (children in index order);
-//    when a node's parent is not the node just processed, each thread
-//    reloads its rows of the parent's checkpoint, which it wrote itself
-//    (same thread, same addresses: program order makes it visible; the
-//    slot is still in L2). Outputs stay indexed by node.
+//  * Tree: nodes run in depth-first preorder, children in ascending order of
+//    subtree size. When a node's parent is not the node just processed, each
+//    thread reloads its rows of the parent's checkpoint, which it wrote
+//    itself (same thread, same addresses: program order makes it visible;
+//    the order keeps the slot in L2). The root's rows, needed again by its
+//    later children, are parked in tensor memory (each thread's own lane)
+//    instead of being re-read from DRAM. Outputs stay indexed by node.
 #include <cuda_runtime.h>
 
 #include <atomic>
