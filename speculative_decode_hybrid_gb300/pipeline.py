@@ -159,16 +159,27 @@ class SpecStep:
         else:
             G.gdn_verify_span_wy(d, self.n_tok, x, a, b, w, S, Cs, self.out[bs, ys], self.dev_status, stream)
 
-    def blocks(self, n: int = 4):
-        """Up to n contiguous (b0, b1, y0, y1) blocks covering every request
-        and layer, in item order: layer ranges for one request, request
-        ranges otherwise."""
+    def blocks(self, n=4):
+        """Contiguous (b0, b1, y0, y1) blocks covering every request and
+        layer, in item order: layer ranges for one request, request ranges
+        otherwise. n: a number of (nearly) equal blocks, or a list of
+        relative block sizes (e.g. [1, 3, 8]: small first, growing)."""
         B, Y = self.shape.batch, self.shape.layers
+        total = Y if B == 1 else B
+        if isinstance(n, int):
+            n = max(1, min(n, total))
+            cuts = [k * total // n for k in range(n + 1)]
+        else:
+            w = [float(v) for v in n]
+            acc, cuts = 0.0, [0]
+            for v in w:
+                acc += v
+                cuts.append(int(round(acc / sum(w) * total)))
+            cuts = sorted(set(min(total, max(0, c)) for c in cuts) | {0, total})
+        spans = [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
         if B == 1:
-            n = max(1, min(n, Y))
-            return [(0, 1, k * Y // n, (k + 1) * Y // n) for k in range(n)]
-        n = max(1, min(n, B))
-        return [(k * B // n, (k + 1) * B // n, 0, Y) for k in range(n)]
+            return [(0, 1, a, b) for a, b in spans]
+        return [(a, b, 0, Y) for a, b in spans]
 
     # -- per-layer launches: how a model whose layers run in sequence calls it
     def verify_per_layer(self, stream=None):
@@ -235,13 +246,16 @@ class SpecStep:
         """One captured step on the current stream (capture() first)."""
         self._graph.replay()
 
-    def capture_host_step(self, host: dict, out_host: dict, commit: str = "checkpoint", chunks: int = 4):
+    def capture_host_step(self, host: dict, out_host: dict, commit: str = "checkpoint", chunks=(1, 3, 8)):
         """Capture the end-to-end step for fixed pinned host buffers (see
         run_host_step) into one CUDA graph that pipelines the host link with
         the verify:
-        - a copy branch DMAs x, a, b in `chunks` contiguous blocks in item
-          order (blocks(): layer ranges for one request, request ranges
-          otherwise), then logits, tokens (and parent);
+        - a copy branch DMAs x, a, b in contiguous blocks in item order
+          (blocks(chunks): layer ranges for one request, request ranges
+          otherwise), then logits, tokens (and parent). The default sizes
+          1 : 3 : 8 expose only a small first copy while each later block
+          lands before the verify needs it (48 layers: 4, 12, 32 layers;
+          this beat 4 equal blocks by 2-4 %, 2 and 5 blocks too);
         - the verify of each block is its own launch on its own branch, and
           starts as soon as its block has landed (the blocks' layers and
           requests are independent), so only the first block's copy is
