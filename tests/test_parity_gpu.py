@@ -186,6 +186,21 @@ def test_gpu_tree_that_is_a_chain_equals_chain():
     assert torch.equal(chain.ssm_state, tree.ssm_state)
 
 
+def test_gpu_tree_many_root_children_d64_big_launch():
+    """A launch big enough for 128-row items (10 layers x 32 heads): the tree
+    instantiation that parks the root's rows in tensor memory, at d_k = 64,
+    with a root of five children (four restarts from the parked rows), and
+    every layer checked against the oracle."""
+    s = shape(h_k=16, h_v=32, d_k=64, d_v=64, layers=10, n_nodes=12, tree=True)
+    wl = W.draw(s, seed=61)
+    par = np.array([[-1, 0, 0, 0, 1, 1, 2, 0, 4, 0, 9, 3]], dtype=np.int32)
+    wl = dataclasses.replace(wl, parent=par)
+    st = run(wl)
+    for y, ref in enumerate(oracle.verify_request(wl, 0)):
+        check_layer_vs_oracle(st, wl, 0, y, ref)
+    assert int(st.dev_status.item()) == 0
+
+
 def test_gpu_deterministic():
     wl = W.make_workload(3, seed=8, layers=4)
     a = run(wl)
