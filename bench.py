@@ -233,7 +233,7 @@ def run_ours(args):
     if replay and st.tree:
         raise SystemExit("the replay commit is defined for chains only")
     st.commit = args.commit
-    f_verify = {"checkpoint": st.verify, "replay": st.verify_nockpt, "wy": st.verify_wy}[args.commit]
+    f_verify = {"checkpoint": st.verify, "replay": st.verify_nockpt_fastest, "wy": st.verify_wy}[args.commit]
     f_commit = {"checkpoint": st.restore, "replay": st.commit_replay, "wy": st.commit_wy}[args.commit]
     step_fn = st.step_fn(args.commit)
     stream = torch.cuda.current_stream(dev)
@@ -345,7 +345,8 @@ def run_ours(args):
         "config": config_of(st, wl, kl),
         "roofline": {"bound": "hbm",
                      "kernel": {"checkpoint": "gdn_verify_persistent (gdn_verify_span)",
-                                "replay": "gdn_verify_persistent (gdn_verify_span_nockpt)",
+                                "replay": ("gdn_wy_kernel (gdn_verify_span_wy)" if st.n_tok <= 16
+                                           else "gdn_verify_persistent (gdn_verify_span_nockpt)"),
                                 "wy": "gdn_wy_kernel (gdn_verify_span_wy)"}[args.commit],
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": peak_kind, "traffic": None if replay else recorded_traffic(),

@@ -97,9 +97,20 @@ class SpecStep:
         G.gdn_commit_replay(self.dims, self.n_tok, self.accept_len, self.x, self.a, self.b, self.conv_w,
                             self.ssm_state, self.conv_state, self.dev_status, stream)
 
+    def verify_nockpt_fastest(self, stream=None):
+        """The faster of the two checkpoint-free verifies: the chunked form
+        (tensor-core product) for spans it takes, else the rank-1 kernel.
+        Their o agree to f32 rounding, and the state they leave is the same
+        (neither writes it)."""
+        if self.n_tok <= G.GDN_WY_MAX_TOKENS:
+            self.verify_wy(stream)
+        else:
+            self.verify_nockpt(stream)
+
     def step_replay(self, stream=None):
-        """verify (no checkpoints) -> accept -> replay the accepted tokens."""
-        self.verify_nockpt(stream)
+        """verify (no checkpoints) -> accept -> replay the accepted tokens
+        (rank-1, from the live state)."""
+        self.verify_nockpt_fastest(stream)
         self.accept(stream)
         self.commit_replay(stream)
 
@@ -135,8 +146,9 @@ class SpecStep:
     def verify_block(self, b0: int, b1: int, y0: int, y1: int, kind: str = "checkpoint", stream=None):
         """The verify of requests [b0, b1) x layers [y0, y1) as one launch.
         The slices of the [B][Y] layouts must be contiguous: all layers, or
-        one request. kind: "checkpoint", "replay" (no checkpoints, rank-1)
-        or "wy" (no checkpoints, chunked form)."""
+        one request. kind: "checkpoint", "replay" (no checkpoints: the
+        faster form, as verify_nockpt_fastest) or "wy" (no checkpoints,
+        chunked form)."""
         s = self.shape
         if not (y0 == 0 and y1 == s.layers) and b1 - b0 != 1:
             raise ValueError("a layer range is contiguous for one request only")
@@ -154,7 +166,7 @@ class SpecStep:
             else:
                 G.gdn_verify_span(d, self.n_tok, x, a, b, w, S, Cs, self.ssm_ckpt[bs, ys],
                                   self.conv_ckpt[bs, ys], self.out[bs, ys], self.dev_status, stream)
-        elif kind == "replay":
+        elif kind == "replay" and self.n_tok > G.GDN_WY_MAX_TOKENS:
             G.gdn_verify_span_nockpt(d, self.n_tok, x, a, b, w, S, Cs, self.out[bs, ys], self.dev_status, stream)
         else:
             G.gdn_verify_span_wy(d, self.n_tok, x, a, b, w, S, Cs, self.out[bs, ys], self.dev_status, stream)
