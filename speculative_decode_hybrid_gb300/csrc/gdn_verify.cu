@@ -387,7 +387,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
 //
 // SL: slots of 4 rows per warp in the recurrence (4 by default, 1 for small
 // launches, whose items have few rows).
-template <int DK, bool BF16, bool TREE, int KT, int SL>
+//
+// RP (chains): the replay commit. An item runs only the first
+// k = accept_len[request] tokens, from the live state, without checkpoints
+// or outputs, and writes its rows' final state back over the live state
+// (k = 0: untouched). The staged prologue then covers those k tokens only.
+template <int DK, bool BF16, bool TREE, int KT, int SL, bool RP = false>
 __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const VerifyArgs p, int n_items) {
     constexpr int ES = BF16 ? 2 : 4;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -432,15 +437,29 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     int pr = 0;
     int tables_of = -1;  // request whose tree tables are in shared memory
     bool reuse_qk = false;  // q_s / k_s / kq_s hold this item's normalised q, k
+    // the tokens an item runs: all of them, or (replay) the accepted ones
+    auto tokens_of = [&](const Item &J) -> int {
+        if constexpr (!RP) return T;
+        const int k = p.accept_len[J.bidx];
+        return k >= 0 && k <= T ? k : 0;  // out of range: flagged below, nothing changes
+    };
+    VerifyArgs pn = p;  // p with T = the staged item's tokens
     {
         const Item I0 = decode_item(p, it, nrb);
-        prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads);
+        pn.T = tokens_of(I0);
+        prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, pn.T);
         prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr, tid);
     }
     while (true) {
         if (tid == 0 && stealing) steal_issue(resp, bar);  // the next item, answered during this prologue
         const Item I = decode_item(p, it, nrb);
-        const bool has_rows = warp * RowState<DK, SL>::kRows < I.R;
+        const VerifyArgs pi = pn;  // this item's token count (pn moves on to the next item)
+        if constexpr (RP) {
+            const int k = p.accept_len[I.bidx];
+            if ((k < 0 || k > T) && p.dev_status && tid == 0 && I.y == 0 && I.h == 0 && I.rb == 0)
+                atomicOr(p.dev_status, GDN_DEV_NODE_RANGE);
+        }
+        const bool has_rows = warp * RowState<DK, SL>::kRows < I.R && pi.T > 0;
         const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
         RowState<DK, SL> rs;
         load_rows(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
@@ -459,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             }
         }
 
-        conv_staged<DK, BF16, TREE, KT>(p, I, xst, wst, cst, src_s, q_s, k_s, v_s, reuse_qk, tid, nthreads);
+        conv_staged<DK, BF16, TREE, KT>(pi, I, xst, wst, cst, src_s, q_s, k_s, v_s, reuse_qk, tid, nthreads);
         if (tid == 0) {
             int nx = -1;
             if (stealing) {
@@ -478,19 +497,28 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         if (next < n_items) {
             const Item In = decode_item(p, next, nrb);
             next_reuse = In.by == I.by && In.g == I.g;
-            prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads);
+            pn.T = tokens_of(In);
+            prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads, pn.T);
             prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
         }
-        if (!reuse_qk) norm_qk<DK>(p, q_s, k_s, kq_s, p.T, threadIdx.x >> 5, blockDim.x >> 5);
+        if (!reuse_qk) norm_qk<DK>(pi, q_s, k_s, kq_s, pi.T, threadIdx.x >> 5, blockDim.x >> 5);
         __syncthreads();
         if (has_rows) {
             float *ck0 =
                 p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-            recurrence<DK, TREE, SL, kPark>(p, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
+            recurrence<DK, TREE, SL, kPark>(pi, rs, p.ssm_in + head_off, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s,
                                             par_s, kPark ? park_s : 0u);
+            if constexpr (RP) {  // the rows after token k-1 replace the live rows (each thread its own)
+                const int j8 = (tid & 31) & (kLanesPerRow - 1);
+#pragma unroll
+                for (int s2 = 0; s2 < SL; ++s2)
+#pragma unroll
+                    for (int m = 0; m < RowState<DK, SL>::NV4; ++m)
+                        st4(p.ssm_out + head_off + (size_t)rs.lrow[s2] * DK + 4 * j8 + kColStride * m, rs.S[s2][m]);
+            }
         }
         __syncthreads();
-        write_out(p, I, o_s, threadIdx.x, blockDim.x);
+        if constexpr (!RP) write_out(p, I, o_s, threadIdx.x, blockDim.x);
         if (next >= n_items) break;
         it = next;
         reuse_qk = next_reuse;
@@ -640,6 +668,28 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// The replay commit on the work-stealing kernel (chains): returns GDN_OK when
+// launched, 1 when the shape or the inputs' alignment calls for the
+// one-item-per-CTA replay kernel instead.
+template <int DK, bool BF16>
+int launch_replay(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStream_t stream) {
+    const int rows = a.d_v < kRowsPerCta ? a.d_v : kRowsPerCta;
+    const int threads = rows / kRowsPerWarp * 32;
+    const PipeLayout Lp = make_pipe_layout(a.T, DK, a.K, BF16 ? 2 : 4);
+    if (!(aligned_inputs && Lp.total + kStaticSmem <= kMaxSmem && threads > a.T)) return 1;
+    VerifyArgs pa = a;
+    const int sms = gdnhost::sm_count();
+    const long long want = 2LL * (sms > 0 ? sms : 152);
+    while (pa.rpi > kRowsPerWarp && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
+    auto kern = a.K == 4 ? gdn_verify_persistent<DK, BF16, false, 4, kSlots, true>
+                         : gdn_verify_persistent<DK, BF16, false, 0, kSlots, true>;
+    static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
+    if (!ensure_smem(kern, Lp.total, a.K == 4 ? set4 : set0)) return GDN_ERR_CUDA;
+    const int grid = batch * a.Y * a.H_v * row_blocks(pa);
+    return launch_pdl(kern, dim3(grid), dim3(threads), Lp.total, stream, pa, grid) == cudaSuccess ? GDN_OK
+                                                                                                   : GDN_ERR_CUDA;
+}
+
 template <bool TREE>
 int dispatch_verify(const gdn_dims *d, const VerifyArgs &a, cudaStream_t stream) {
     const bool bf = d->in_dtype == GDN_BF16;
@@ -743,6 +793,7 @@ extern "C" int gdn_commit_replay(const gdn_dims *d, int32_t n_tok, const int32_t
     VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_state, conv_state, nullptr, nullptr, nullptr,
                              nullptr, dev_status);
     v.ssm_out = ssm_state;
+    v.accept_len = accept_len_dev;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int nrb = row_blocks(v);
     const int rows = d->d_v < kRowsPerCta ? d->d_v : kRowsPerCta;
@@ -750,18 +801,27 @@ extern "C" int gdn_commit_replay(const gdn_dims *d, int32_t n_tok, const int32_t
     const Layout L = make_layout(n_tok, d->d_k, d->conv_k);
     const dim3 grid(nrb, d->h_v, d->batch * d->layers);
     const bool bf = d->in_dtype == GDN_BF16;
-    if (d->d_k == 128) {
-        auto kern = bf ? gdn_replay_kernel<128, true> : gdn_replay_kernel<128, false>;
-        static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
-        if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
-        if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
-            return GDN_ERR_CUDA;
-    } else {
-        auto kern = bf ? gdn_replay_kernel<64, true> : gdn_replay_kernel<64, false>;
-        static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
-        if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
-        if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
-            return GDN_ERR_CUDA;
+    // the staged work-stealing kernel when the inputs allow cp.async staging
+    const bool al = aligned16(x) && aligned16(conv_w);
+    if (d->d_k == 128)
+        rc = bf ? launch_replay<128, true>(v, d->batch, al, st) : launch_replay<128, false>(v, d->batch, al, st);
+    else
+        rc = bf ? launch_replay<64, true>(v, d->batch, al, st) : launch_replay<64, false>(v, d->batch, al, st);
+    if (rc != GDN_OK && rc != 1) return rc;
+    if (rc == 1) {  // the one-item-per-CTA replay kernel: inputs loaded directly
+        if (d->d_k == 128) {
+            auto kern = bf ? gdn_replay_kernel<128, true> : gdn_replay_kernel<128, false>;
+            static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
+            if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
+            if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
+                return GDN_ERR_CUDA;
+        } else {
+            auto kern = bf ? gdn_replay_kernel<64, true> : gdn_replay_kernel<64, false>;
+            static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
+            if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
+            if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
+                return GDN_ERR_CUDA;
+        }
     }
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     if (d->conv_k > 1) {

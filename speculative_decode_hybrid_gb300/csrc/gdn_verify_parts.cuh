@@ -37,6 +37,7 @@ struct VerifyArgs {
     const int32_t *parent;  // [B][T+1] for trees, nullptr for chains
     int32_t *dev_status;
     float *ssm_out;         // replay commit: the live state, updated in place
+    const int32_t *accept_len;  // replay commit: tokens to replay per request
     int rpi;                // value rows per work item: a multiple of 16, <= kRowsPerCta
 };
 
@@ -284,10 +285,11 @@ __device__ __forceinline__ float conv_out(const float (&wr)[GDN_MAX_CONV_K], con
 // into the staging buffers (16-byte cp.async; every source and destination
 // offset is a multiple of 16 bytes, see the host-side eligibility check).
 // with_qk false: the v range only (the q/k of the item are already on chip).
+// ntok: the tokens to copy (the first ntok of the span, ntok <= p.T).
 template <int DK, bool BF16>
 __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I, unsigned char *xst,
                                               unsigned char *wst, unsigned char *cst, bool with_qk, int tid,
-                                              int nthreads) {
+                                              int nthreads, int ntok) {
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int XS = 2 * DK + kRowsPerCta;
     const int T = p.T, K = p.K;
@@ -300,7 +302,7 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
     {
         const int cq = DK * ES / 16, cv = I.R * ES / 16;
         const int r0 = with_qk ? 0 : 2 * cq, per_node = 2 * cq + cv - r0;
-        for (int i = tid; i < T * per_node; i += nthreads) {
+        for (int i = tid; i < ntok * per_node; i += nthreads) {
             const int t = i / per_node, r = r0 + (i - t * per_node);
             size_t c0;
             int dch, off;
@@ -500,6 +502,7 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
     v.parent = parent;
     v.dev_status = dev_status;
     v.ssm_out = nullptr;
+    v.accept_len = nullptr;
     v.rpi = kRowsPerCta;
     return v;
 }

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     const float *s_in = (COMMIT ? p.ssm_out : p.ssm_in) + head_off;
 
     // staged inputs (first cp.async group), then the state tile (second group)
-    prefetch_item<DK, BF16>(p, I, xst, wst, cst, true, tid, nthreads);
+    prefetch_item<DK, BF16>(p, I, xst, wst, cst, true, tid, nthreads, p.T);
     float ga = 0.f, gb = 0.f;
     int pr = 0;
     prefetch_scalars<BF16, false>(p, I, ga, gb, pr, tid);
