@@ -3,7 +3,7 @@
 // split SSM and convolution state on-device; lucebox PR #506, Summary: fast
 // rollback from F32 checkpoints, no replay).
 //
-// grid (chunks, B*Y), sized for 8 resident CTAs per SM (64 warps): every CTA
+// grid (chunks, B*Y), at most one wave of 8 resident CTAs per SM: every CTA
 // reads the accepted node of its request from device memory (no host round
 // trip), returns at once for node 0 (verify never touched the live state)
 // and otherwise copies its share of the 16-byte vectors of slot node-1, 4
@@ -94,7 +94,7 @@ extern "C" int gdn_rollback_restore(const gdn_dims *d, int32_t n_tok, const int3
     const int rows = d->batch * d->layers;
     const int sms = gdnhost::sm_count();
     const int target = kCtasPerSm * (sms > 0 ? sms : 152);
-    int chunks = (target + rows - 1) / rows;
+    int chunks = target / rows;  // one wave: a second, partial wave would run after the first
     const size_t per_cta_min = (size_t)kThreads * kUnroll;  // float4 per CTA, at least one full round
     const size_t max_chunks = (ssm_slot / 4 + per_cta_min - 1) / per_cta_min;
     if ((size_t)chunks > max_chunks) chunks = (int)max_chunks;

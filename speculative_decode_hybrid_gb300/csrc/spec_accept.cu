@@ -28,6 +28,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxSplits = 64;
+constexpr int kLoads = 4;                        // float4 loads in flight per thread
+constexpr int kRoundLogits = kThreads * kLoads * 4;  // logits one CTA covers in one round
 constexpr int kMaxNodes = GDN_MAX_TOKENS + 1;
 static_assert(kMaxNodes <= kThreads, "one thread per node");
 constexpr size_t kCounterBytes(int32_t batch) { return (((size_t)batch * 4 + 255) / 256) * 256; }
@@ -70,16 +72,26 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
 
     unsigned long long best = 0ull;  // below every real element
     if ((V & 3) == 0) {
+        // rounds of kLoads independent 16-byte loads per thread, all issued
+        // before the first is used (one chunk is normally a single round)
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
         const int lo4 = lo >> 2, hi4 = hi >> 2;  // lo is a multiple of 4
-#pragma unroll 4
-        for (int i = lo4 + tid; i < hi4; i += kThreads) {
-            const float4 f = __ldcs(r4 + i);
-            const unsigned base = (unsigned)i * 4u;
-            best = umax64(best, make_key(f.x, base));
-            best = umax64(best, make_key(f.y, base + 1));
-            best = umax64(best, make_key(f.z, base + 2));
-            best = umax64(best, make_key(f.w, base + 3));
+        for (int i0 = lo4 + tid; i0 < hi4; i0 += kLoads * kThreads) {
+            float4 f[kLoads];
+#pragma unroll
+            for (int u = 0; u < kLoads; ++u)
+                if (i0 + u * kThreads < hi4) f[u] = __ldcs(r4 + i0 + u * kThreads);
+#pragma unroll
+            for (int u = 0; u < kLoads; ++u) {
+                const int i = i0 + u * kThreads;
+                if (i < hi4) {
+                    const unsigned base = (unsigned)i * 4u;
+                    best = umax64(best, make_key(f[u].x, base));
+                    best = umax64(best, make_key(f[u].y, base + 1));
+                    best = umax64(best, make_key(f[u].z, base + 2));
+                    best = umax64(best, make_key(f[u].w, base + 3));
+                }
+            }
         }
     } else {
         for (int i = lo + tid; i < hi; i += kThreads) best = umax64(best, make_key(__ldcs(row + i), (unsigned)i));
@@ -166,12 +178,16 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     }
 }
 
+// Chunks per logit row: enough that a chunk is one round of loads (the scan
+// is then a single memory round trip), and, for few rows, enough CTAs to
+// cover the SMs, down to ~2K logits per chunk.
 int choose_splits(int rows, int V) {
     const int sms = gdnhost::sm_count();
     const int target = 4 * (sms > 0 ? sms : 152);
-    int s = (target + rows - 1) / rows;
-    const int by_size = (V + 2047) / 2048;  // at least ~2K logits per CTA
-    if (s > by_size) s = by_size;
+    int s = (V + kRoundLogits - 1) / kRoundLogits;
+    const int by_sms = (target + rows - 1) / rows;
+    const int by_size = (V + 2047) / 2048;
+    if (s < by_sms) s = by_sms < by_size ? by_sms : by_size;
     if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
     return s;
