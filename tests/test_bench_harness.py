@@ -57,4 +57,29 @@ def test_reference_arm_prints_the_contract_line():
         assert key in line, key
     assert line["steps"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    # the 4 sampled layers run on at most 4 threads
+    assert line["cpu_baseline"]["kind"] == "oracle" and 1 <= line["cpu_baseline"]["cores"] <= 4
+
+
+def test_threaded_oracle_step_equals_sequential():
+    # the cpu_baseline runs the oracle's layers on a thread pool: the results
+    # must be those of the sequential loop, bit for bit
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+    from speculative_decode_hybrid_gb300 import workloads as W
+    oracle.build()
+    wl = W.make_workload(0, seed=3, layers=6)
+    layers = list(range(6))
+    seq = oracle.verify_request(wl, 0, layers=layers)
+    with ThreadPoolExecutor(max_workers=4) as pool:
+        par = list(pool.map(lambda y: oracle.verify_request(wl, 0, layers=[y])[0], layers))
+    for a, b in zip(seq, par):
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+    # and the full step (verify + accept + restore) runs through the pool
+    with ThreadPoolExecutor(max_workers=4) as pool:
+        k_pool = bench.oracle_full_step(wl, layers, pool=pool)
+    assert k_pool == bench.oracle_full_step(wl, layers)
