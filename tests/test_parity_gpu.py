@@ -685,8 +685,10 @@ def test_wy_rejects_long_spans():
 
 @pytest.mark.parametrize("tree", [False, True])
 def test_per_layer_launches_equal_one_launch(tree):
-    """One verify launch per layer gives, bit for bit, the all-layers launch."""
-    wl = W.make_workload(3 if tree else 2, seed=12, layers=3)
+    """One verify launch per layer gives, bit for bit, the all-layers launch.
+    12 layers: the all-layers launch has whole 128-row items (16 rows per
+    warp); a one-layer launch has 32-row items (4 rows per warp)."""
+    wl = W.make_workload(3 if tree else 2, seed=12, layers=12)
     a, b = SpecStep(wl), SpecStep(wl)
     a.verify()
     b.verify_per_layer()
