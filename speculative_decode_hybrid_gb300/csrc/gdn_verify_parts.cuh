@@ -232,57 +232,37 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
 template <int DK>
 __device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s, int count,
                                        int warp, int nwarps) {
-    // two nodes per pass (t and t + nwarps): their reductions interleave
     constexpr int PER = DK / 32;
     const int lane = threadIdx.x & 31;
-    for (int t = warp; t < count; t += 2 * nwarps) {
-        const int tt[2] = {t, t + nwarps};
-        const bool two = tt[1] < count;
-        float qv[2][PER], kv[2][PER];
-        float sq[2] = {0.f, 0.f}, sk[2] = {0.f, 0.f};
+    for (int t = warp; t < count; t += nwarps) {
+        float qv[PER], kv[PER];
+        float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            if (n == 1 && !two) break;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) {
-                qv[n][e] = q_s[(size_t)tt[n] * DK + lane + 32 * e];
-                kv[n][e] = k_s[(size_t)tt[n] * DK + lane + 32 * e];
-                sq[n] = fmaf(qv[n][e], qv[n][e], sq[n]);
-                sk[n] = fmaf(kv[n][e], kv[n][e], sk[n]);
-            }
+        for (int e = 0; e < PER; ++e) {
+            qv[e] = q_s[(size_t)t * DK + lane + 32 * e];
+            kv[e] = k_s[(size_t)t * DK + lane + 32 * e];
+            sq = fmaf(qv[e], qv[e], sq);
+            sk = fmaf(kv[e], kv[e], sk);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                sq[n] += __shfl_xor_sync(0xffffffffu, sq[n], off);
-                sk[n] += __shfl_xor_sync(0xffffffffu, sk[n], off);
-            }
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
         }
-        float kq[2] = {0.f, 0.f};
+        const float iq = 1.0f / sqrtf(sq + 1e-6f);
+        const float ik = 1.0f / sqrtf(sk + 1e-6f);
+        float kq = 0.f;
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            if (n == 1 && !two) break;
-            const float iq = 1.0f / sqrtf(sq[n] + 1e-6f);
-            const float ik = 1.0f / sqrtf(sk[n] + 1e-6f);
-#pragma unroll
-            for (int e = 0; e < PER; ++e) {
-                qv[n][e] = qv[n][e] * iq * p.q_scale;
-                kv[n][e] = kv[n][e] * ik;
-                q_s[(size_t)tt[n] * DK + lane + 32 * e] = qv[n][e];
-                k_s[(size_t)tt[n] * DK + lane + 32 * e] = kv[n][e];
-                kq[n] = fmaf(qv[n][e], kv[n][e], kq[n]);
-            }
+        for (int e = 0; e < PER; ++e) {
+            qv[e] = qv[e] * iq * p.q_scale;
+            kv[e] = kv[e] * ik;
+            q_s[(size_t)t * DK + lane + 32 * e] = qv[e];
+            k_s[(size_t)t * DK + lane + 32 * e] = kv[e];
+            kq = fmaf(qv[e], kv[e], kq);
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) kq[n] += __shfl_xor_sync(0xffffffffu, kq[n], off);
-        }
-        if (lane == 0) {
-            kq_s[tt[0]] = kq[0];
-            if (two) kq_s[tt[1]] = kq[1];
-        }
+        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        if (lane == 0) kq_s[t] = kq;
     }
 }
 
