@@ -50,15 +50,6 @@ __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast
 
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 
-// 16-byte store that marks the line evict-first in L2: checkpoint slots are
-// written once and read at most once (by the restore of one slot).
-__device__ __forceinline__ void st4_stream(float *p, float4 v) {
-    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :
-                 : "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     acc = fmaf(a.x, b.x, acc);
     acc = fmaf(a.y, b.y, acc);
