@@ -41,11 +41,16 @@ METRIC = "GDN verify+rollback tokens·layers/s (span 16, 48 layers); % of HBM ro
 UNIT = "tokens*layers/s"
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "speculative_decode_hybrid_gb300", "csrc")
 # the verify kernel's sources, hashed together (in this order) to tie the
 # recorded ncu traffic to the code it was taken with
-VERIFY_SRCS = [os.path.join(ROOT, "speculative_decode_hybrid_gb300", "csrc", f)
-               for f in ("gdn_verify.cu", "gdn_verify_parts.cuh", "gdn_device.cuh")]
+VERIFY_SRCS = [os.path.join(CSRC, f) for f in ("gdn_verify.cu", "gdn_verify_parts.cuh", "gdn_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_verify_kernel_traffic.txt")
+# one full-size ncu capture each: (workload, layers, verify kind) -> DRAM bytes
+# of one verify launch, with the kernel sources it was taken at
+TRAFFIC_FILES = [TRAFFIC_FILE,
+                 os.path.join(ROOT, "profiles", "gdn_tree_verify_traffic.txt"),
+                 os.path.join(ROOT, "profiles", "gdn_wy_kernel_traffic.txt")]
 
 
 def parse():
@@ -89,26 +94,40 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per verify launch from the committed ncu summary, or None
-    when the kernel source changed since the counters were taken."""
-    try:
-        vals = {}
-        with open(TRAFFIC_FILE) as f:
-            for line in f:
-                if ":" in line and not line.startswith("#"):
-                    k, v = line.split(":", 1)
-                    vals[k.strip()] = v.strip()
-        h = hashlib.sha256()
-        for src in VERIFY_SRCS:
-            with open(src, "rb") as f:
-                h.update(f.read())
-        sha = h.hexdigest()
-        if vals.get("source_sha256") != sha:
-            return None
-        return int(vals["dram_bytes_per_launch"])
-    except Exception:
-        return None
+def read_traffic_file(path):
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    return vals
+
+
+def sources_sha(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload=2, layers=48, kind="checkpoint"):
+    """DRAM bytes per verify launch from the committed ncu summary of this
+    workload, layer count and verify kind ("checkpoint" or "chunked"), or
+    None when there is none or the kernel source changed since the counters
+    were taken."""
+    for path in TRAFFIC_FILES:
+        try:
+            vals = read_traffic_file(path)
+            if (int(vals["workload"]), int(vals["layers"]), vals["verify"]) != (workload, layers, kind):
+                continue
+            if vals.get("source_sha256") != sources_sha(vals["sources"].split()):
+                return None
+            return int(vals["dram_bytes_per_launch"])
+        except (OSError, KeyError, ValueError):
+            continue
+    return None
 
 
 class ClockSampler:
@@ -319,6 +338,8 @@ def run_ours(args):
 
     hbm, peak_kind = peaks()
     vbytes = st.verify_bytes() if not replay else st.replay_bytes(np.zeros(st.shape.batch, dtype=int)) - st.accept_bytes()
+    # the kernel timed: checkpointing, or the chunked checkpoint-free one (chain spans <= 16)
+    verify_kind = "checkpoint" if not replay else ("chunked" if st.n_tok <= 16 and not st.tree else "other")
     ver_mean_s = statistics.mean(ver_ms) / 1e3
     achieved = vbytes / ver_mean_s / 1e9
     step_bytes = (vbytes + st.accept_bytes() + st.restore_bytes(kn)) if not replay else st.replay_bytes(kl)
@@ -344,12 +365,13 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(st, wl, kl),
         "roofline": {"bound": "hbm",
-                     "kernel": {"checkpoint": "gdn_verify_persistent (gdn_verify_span)",
+                     "kernel": {"checkpoint": "gdn_verify_persistent (%s)" % (
+                                    "gdn_tree_verify" if st.tree else "gdn_verify_span"),
                                 "replay": ("gdn_wy_kernel (gdn_verify_span_wy)" if st.n_tok <= 16
                                            else "gdn_verify_persistent (gdn_verify_span_nockpt)"),
                                 "wy": "gdn_wy_kernel (gdn_verify_span_wy)"}[args.commit],
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": peak_kind, "traffic": None if replay else recorded_traffic(),
+                     "peak_source": peak_kind, "traffic": recorded_traffic(BENCH_WID, st.shape.layers, verify_kind),
                      "algorithmic_bytes_per_launch": vbytes,
                      "verify_us_mean": ver_mean_s * 1e6,
                      "verify_us_median": statistics.median(ver_ms) * 1e3,

@@ -83,3 +83,21 @@ def test_threaded_oracle_step_equals_sequential():
     with ThreadPoolExecutor(max_workers=4) as pool:
         k_pool = bench.oracle_full_step(wl, layers, pool=pool)
     assert k_pool == bench.oracle_full_step(wl, layers)
+
+
+def test_recorded_traffic_is_per_workload_and_kernel():
+    # each committed capture names its workload, layers, verify kind and
+    # sources; the traffic is reported only for that configuration, and only
+    # while the sources hash to the recorded value
+    seen = set()
+    for path in bench.TRAFFIC_FILES:
+        vals = bench.read_traffic_file(path)
+        key = (int(vals["workload"]), int(vals["layers"]), vals["verify"])
+        assert key not in seen
+        seen.add(key)
+        got = bench.recorded_traffic(*key)
+        fresh = vals["source_sha256"] == bench.sources_sha(vals["sources"].split())
+        assert got == (int(vals["dram_bytes_per_launch"]) if fresh else None)
+        assert int(vals["dram_bytes_per_launch"]) == int(vals["dram_bytes_read"]) + int(vals["dram_bytes_write"])
+    assert bench.recorded_traffic(4, 48, "checkpoint") is None
+    assert bench.recorded_traffic(2, 12, "checkpoint") is None
