@@ -211,18 +211,37 @@ def aggregate(local_time, local_units, ws, device):
     return float(t.item()), float(u.item())
 
 
-def config_of(st, wl, kl):
+def verify_footprint_bytes(s):
+    """Bytes one verify of shape s moves (state and conv state read, every
+    checkpoint written, inputs read, o written, conv weights read)."""
+    T, C, K = s.n_tok, s.conv_ch, s.conv_k
+    el = 2 if s.dtype == 1 else 4
+    per = ((T + 1) * (s.h_v * s.d_v * s.d_k * 4 + C * (K - 1) * 4)
+           + T * C * el + 2 * T * s.h_v * el + T * s.h_v * s.d_v * 4)
+    return s.batch * s.layers * per + s.layers * C * K * el
+
+
+def config_of(wl, kl, commit="checkpoint", l2=None):
+    """The workload's config dict; both arms print it, so that the two lines
+    can be matched key by key (only `l2`, how the GPU arm keeps the L2 cold,
+    is the arm's own)."""
     s = wl.shape
     from speculative_decode_hybrid_gb300.workloads import WORKLOAD_NAMES
+    if l2 is None:
+        l2 = ("256 MiB buffer written between timed steps (outside the events); "
+              "step footprint %.2f GiB" % (verify_footprint_bytes(s) / 2 ** 30))
     return {"workload": WORKLOAD_NAMES.get(BENCH_WID, "custom"), "batch": s.batch, "layers": s.layers,
             "span": s.n_tok, "tree_nodes": s.n_nodes if s.tree else None,
             "h_k": s.h_k, "h_v": s.h_v, "d_k": s.d_k, "d_v": s.d_v, "conv_channels": s.conv_ch,
             "conv_k": s.conv_k, "vocab": s.vocab, "input_dtype": "bf16" if s.dtype == 1 else "f32",
             "state_dtype": "f32", "accepted_len": [int(k) for k in kl], "seed": wl.seed,
-            "l2": "256 MiB buffer written between timed steps (outside the events); "
-                  "step footprint %.2f GiB" % (st.verify_bytes() / 2 ** 30),
+            "l2": l2,
             "parallelism": "replicas (independent requests per rank, no collective)",
-            "commit": getattr(st, "commit", "checkpoint")}
+            "commit": commit}
+
+
+def med_ms(xs):
+    return statistics.median(xs) if xs else None
 
 
 BENCH_WID = 2
@@ -361,9 +380,10 @@ def run_ours(args):
     st.conv_state.copy_(conv0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
-        "warmup": max(3, args.warmup), "ms_per_step": total_max_ms / K, "higher_is_better": True,
+        "warmup": max(3, args.warmup), "ms_per_step": total_max_ms / K,
+        "ms_per_step_median": statistics.median(gstep_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(st, wl, kl),
+        "config": config_of(wl, kl, getattr(st, "commit", "checkpoint")),
         "roofline": {"bound": "hbm",
                      "kernel": {"checkpoint": "gdn_verify_persistent (%s)" % (
                                     "gdn_tree_verify" if st.tree else "gdn_verify_span"),
@@ -376,7 +396,10 @@ def run_ours(args):
                      "verify_us_mean": ver_mean_s * 1e6,
                      "verify_us_median": statistics.median(ver_ms) * 1e3,
                      "accept_us_mean": statistics.mean(acc_ms) * 1e3,
+                     "accept_us_median": statistics.median(acc_ms) * 1e3,
                      "restore_us_mean": statistics.mean(res_ms) * 1e3,
+                     "restore_us_median": statistics.median(res_ms) * 1e3,
+                     "eager_step_us_median": statistics.median(step_ms) * 1e3,
                      "step_bytes": step_bytes, "step_gbs": step_gbs, "step_frac": step_gbs / hbm},
         "e2e": e2e,
         "per_layer": per_layer,
@@ -428,6 +451,7 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
     assert int(out_host["accept_len"][0]) == int(kl[0])
     return {"value": e2e_units / e2e_max_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s),
+            "ms_per_step_median": 1e3 * statistics.median(e2e_s),
             "mode": mode}
 
 
@@ -460,8 +484,10 @@ def run_per_layer(st, flush, dev, stream, K, units, ws):
     st._graph = main_graph
     total_max_ms, units_all = aggregate(sum(step_ms), units * K, ws, dev)
     return {"value": units_all / (total_max_ms / 1e3), "unit": UNIT, "steps": K,
-            "ms_per_step": total_max_ms / K, "launches_per_step": st.shape.layers + 2,
+            "ms_per_step": total_max_ms / K, "ms_per_step_median": statistics.median(step_ms),
+            "launches_per_step": st.shape.layers + 2,
             "verify_us_mean": statistics.mean(ver_ms) * 1e3,
+            "verify_us_median": statistics.median(ver_ms) * 1e3,
             "verify_us_per_layer": statistics.mean(ver_ms) * 1e3 / st.shape.layers,
             "mode": "cuda_graph (step), eager (verify alone)"}
 
@@ -556,18 +582,22 @@ def run_reference(args):
         oracle_full_step(wl, layers, acc, pool=pool)
         times.append(time.perf_counter() - t0)
     pool.shutdown()
+    par = wl.parent[0] if wl.parent is not None else None
+    k_ref = int(oracle.accept_greedy(wl.logits[0], wl.tokens[0], par)[1])
     total = sum(times)
     value = s.n_tok * nl * args.steps / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": W.WORKLOAD_NAMES[BENCH_WID], "layers_per_step_sample": nl,
-                       "seed": wl.seed},
+            "config": config_of(wl, [k_ref], "checkpoint",
+                                l2="CPU arm: host caches, no GPU L2 to flush"),
+            "ms_per_step_median": 1e3 * statistics.median(times),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "each step: %d of %d layers (verify + restore); the acceptance "
                                        "once per %d layers of work; plain C double precision, the "
-                                       "layers on %d threads" % (nl, s.layers, s.layers, cores)},
+                                       "layers on %d threads" % (nl, s.layers, s.layers, cores),
+                             "layers_per_step_sample": nl},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

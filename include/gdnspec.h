@@ -79,6 +79,7 @@ typedef void *gdn_stream_t;
 #define GDN_ERR_TREE_NOT_CHAIN 9  /* a sibling / skipped parent where a pure chain is required */
 #define GDN_ERR_WORKSPACE 10      /* workspace NULL, misaligned or smaller than required */
 #define GDN_ERR_CUDA 11           /* a CUDA launch or query failed */
+#define GDN_ERR_FLAGS 12          /* a flags argument has a bit this library does not define */
 
 /* Device-side status bits, OR-ed into *dev_status (int32, device memory). */
 #define GDN_DEV_TOKEN_RANGE 0x1   /* a draft token id outside [0, vocab): counted as a mismatch */
@@ -146,6 +147,36 @@ int gdn_verify_span(const gdn_dims *dims, int32_t n_tok,
                     int32_t *dev_status, gdn_stream_t stream);
 
 /*
+ * Flags of gdn_verify_span_ex and gdn_tree_verify_ex.
+ *
+ * GDN_VERIFY_STATE_READY — the caller promises that ssm_in, conv_in, conv_w
+ * and (trees) parent_dev are not written by any work on `stream` that may
+ * still be running when this call's kernel starts: with programmatic
+ * dependent launch that is the kernel queued just before the call, whose
+ * tail the verify overlaps (earlier work has completed). The verify then
+ * loads those inputs, and builds its tree tables, before it waits for that
+ * kernel, and only x, a and b (which the previous kernel may produce) after
+ * it. Typical use: the verify of layer y + 1 queued right after the verify
+ * of layer y, as a model whose layers run in sequence calls it; the
+ * previous call writes only layer y's checkpoints and outputs. Not for the
+ * first verify after a restore or commit, which writes the live state. The
+ * results are the same with or without the flag; if the promise is broken,
+ * the verify may read stale state.
+ */
+#define GDN_VERIFY_STATE_READY 0x1u
+
+/*
+ * gdn_verify_span_ex — gdn_verify_span with a flags word (GDN_VERIFY_*;
+ * 0 = gdn_verify_span). Returns, in addition, GDN_ERR_FLAGS for an unknown
+ * bit.
+ */
+int gdn_verify_span_ex(const gdn_dims *dims, int32_t n_tok,
+                       const void *x, const void *a, const void *b, const void *conv_w,
+                       const float *ssm_in, const float *conv_in,
+                       float *ssm_ckpt, float *conv_ckpt, float *out,
+                       int32_t *dev_status, uint32_t flags, gdn_stream_t stream);
+
+/*
  * gdn_tree_verify — verify a DDTree of n_nodes nodes (node 0 = committed
  * root, T = n_nodes - 1 processed nodes) per request. Node i starts from the
  * state of parent(i) and its conv window follows its root path.
@@ -166,6 +197,14 @@ int gdn_tree_verify(const gdn_dims *dims, int32_t n_nodes,
                     const float *ssm_in, const float *conv_in,
                     float *ssm_ckpt, float *conv_ckpt, float *out,
                     int32_t *dev_status, gdn_stream_t stream);
+
+/* gdn_tree_verify_ex — gdn_tree_verify with a flags word, as gdn_verify_span_ex. */
+int gdn_tree_verify_ex(const gdn_dims *dims, int32_t n_nodes,
+                       const int32_t *parent_host, const int32_t *parent_dev,
+                       const void *x, const void *a, const void *b, const void *conv_w,
+                       const float *ssm_in, const float *conv_in,
+                       float *ssm_ckpt, float *conv_ckpt, float *out,
+                       int32_t *dev_status, uint32_t flags, gdn_stream_t stream);
 
 /*
  * spec_accept_greedy — greedy acceptance for a batch of requests.
@@ -220,8 +259,11 @@ size_t spec_accept_workspace_bytes(int32_t batch, int32_t n_nodes);
  * library's device memory, present on every GPU that loads the library until
  * the process exits. The first call on a device (with that device current)
  * looks up the array's device address; make that first call before any
- * stream capture. Every call zeroes the part of the array that must start at
- * zero (a small cudaMemsetAsync on `stream`) and allocates nothing.
+ * stream capture. If the lookup fails, that call returns GDN_ERR_CUDA and
+ * the next call looks again; once found, the address is kept for the life
+ * of the process, so cudaDeviceReset is not supported with this call. Every
+ * call zeroes the part of the array that must start at zero (a small
+ * cudaMemsetAsync on `stream`) and allocates nothing.
  * All calls share the one array: calls that may overlap on the GPU (other
  * streams, other host threads) race and must be serialised by the caller.
  * Returns GDN_ERR_WORKSPACE when spec_accept_workspace_bytes(batch, n_nodes)

@@ -80,6 +80,7 @@ extern "C" const char *gdn_status_str(int status) {
         case GDN_ERR_TREE_NOT_CHAIN: return "tree: sibling or skipped parent where a pure chain is required";
         case GDN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case GDN_ERR_CUDA: return "CUDA launch failed";
+        case GDN_ERR_FLAGS: return "a flags argument has an undefined bit";
         default: return "unknown status";
     }
 }

@@ -422,10 +422,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     const unsigned resp = (unsigned)__cvta_generic_to_shared(steal_s);
     const unsigned bar = resp + 16;
     unsigned phase = 0;
-    bool stealing = true;  // the last request succeeded
+    bool stealing = p.steal != 0;  // the last request succeeded (or: the host found every CTA resident)
     if (tid == 0) steal_init(bar);
     int it = blockIdx.x;
     if (it >= n_items) return;
+    const Item I0 = decode_item(p, it, nrb);
+    RowState<DK, SL> rs;
+    float ga = 0.f, gb = 0.f;
+    int pr = 0;
+    int tables_of = -1;  // request whose tree tables are in shared memory
+    // Before the wait for the previous grid on the stream: with the caller's
+    // promise that this grid does not write them (p.early, never for the
+    // replay commit), the first item's state rows, conv taps, conv state and
+    // (trees) parents are loaded and its tree tables built; everything else
+    // of the item only goes to L2 (a prefetch is safe even for bytes the
+    // previous grid still writes).
+    const bool early = !RP && p.early;
+    prefetch_l2_item<DK, BF16, TREE>(p, I0, tid, nthreads, !early);
+    if (early) {
+        load_rows(rs, p.ssm_in + ((size_t)I0.by * p.H_v + I0.h) * (size_t)p.d_v * DK + (size_t)I0.row0 * DK,
+                  warp * RowState<DK, SL>::kRows < I0.R);
+        prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, T, kStageTaps);
+        if constexpr (TREE) {
+            pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I0.bidx * (T + 1) + tid]) : 0;
+            tree_tables(p, p.parent + (size_t)I0.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0);
+            tables_of = I0.bidx;  // the barrier after the staging wait publishes them
+        }
+    }
     if constexpr (kPark) {
         if (warp == 0) gdntc::tmem_alloc<kParkCols>(&park_s);
         gdntc::fence_before_sync();
@@ -433,9 +456,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         gdntc::fence_after_sync();
     }
     pdl_wait();
-    float ga = 0.f, gb = 0.f;
-    int pr = 0;
-    int tables_of = -1;  // request whose tree tables are in shared memory
+    bool rows_ready = early;  // rs holds the current item's rows already
     bool reuse_qk = false;  // q_s / k_s / kq_s hold this item's normalised q, k
     // the tokens an item runs: all of them, or (replay) the accepted ones
     auto tokens_of = [&](const Item &J) -> int {
@@ -444,12 +465,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         return k >= 0 && k <= T ? k : 0;  // out of range: flagged below, nothing changes
     };
     VerifyArgs pn = p;  // p with T = the staged item's tokens
-    {
-        const Item I0 = decode_item(p, it, nrb);
-        pn.T = tokens_of(I0);
-        prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, pn.T);
-        prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr, tid);
-    }
+    pn.T = tokens_of(I0);
+    prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, pn.T, early ? kStageX : kStageAll);
+    prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr, tid);
     while (true) {
         if (tid == 0 && stealing) steal_issue(resp, bar);  // the next item, answered during this prologue
         const Item I = decode_item(p, it, nrb);
@@ -461,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         }
         const bool has_rows = warp * RowState<DK, SL>::kRows < I.R && pi.T > 0;
         const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-        RowState<DK, SL> rs;
-        load_rows(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
+        if (!rows_ready) load_rows(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
+        rows_ready = false;
 
         cp_async_wait_all();
         if (tid < T) {
@@ -478,18 +496,25 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             }
         }
 
-        conv_staged<DK, BF16, TREE, KT>(pi, I, xst, wst, cst, src_s, q_s, k_s, v_s, reuse_qk, tid, nthreads);
+        conv_norm_staged<DK, BF16, TREE, KT>(pi, I, xst, wst, cst, src_s, q_s, k_s, v_s, kq_s, reuse_qk, warp,
+                                             nthreads >> 5);
         if (tid == 0) {
             int nx = -1;
             if (stealing) {
                 nx = steal_result(resp, bar, phase);
+                // After a give-up the answer may still land (asynchronously,
+                // in this CTA's shared memory): wait once more on the same
+                // phase, so that a late cancellation is still run here and
+                // the CTA does not exit with the write pending. Only when
+                // both waits give up is the item taken as lost.
+                if (nx == -2) nx = steal_result(resp, bar, phase);
                 phase ^= 1u;
                 if (nx == -2 && p.dev_status) atomicOr(p.dev_status, GDN_DEV_SCHED);
                 if (nx < 0 || nx >= n_items) stealing = false;
             }
             next_s = nx;
         }
-        __syncthreads();  // staging consumed; q, k, v ready; next_s set
+        __syncthreads();  // staging consumed; q, k (normalised), k.q, v ready; next_s set
 
         const int next = next_s >= 0 && next_s < n_items ? next_s : n_items;
         if (next >= n_items) pdl_launch_dependents();  // nothing left to take: this CTA's last item
@@ -501,8 +526,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
             prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads, pn.T);
             prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
         }
-        if (!reuse_qk) norm_qk<DK>(pi, q_s, k_s, kq_s, pi.T, threadIdx.x >> 5, blockDim.x >> 5);
-        __syncthreads();
         if (has_rows) {
             float *ck0 =
                 p.ssm_ckpt + ((size_t)I.by * T * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
@@ -650,16 +673,20 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
         auto kern = small ? gdn_verify_persistent<DK, BF16, TREE, 4, 1>
                           : (a.K == 4 ? gdn_verify_persistent<DK, BF16, TREE, 4, kSlots>
                                       : gdn_verify_persistent<DK, BF16, TREE, 0, kSlots>);
-        static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024}, set1{48 * 1024};
-        std::atomic<size_t> &set = small ? set1 : (a.K == 4 ? set4 : set0);
+        static SmemSet set4, set0, set1;
+        SmemSet &set = small ? set1 : (a.K == 4 ? set4 : set0);
         if (!ensure_smem(kern, Lp.total, set)) return GDN_ERR_CUDA;
-        // one CTA per item: the running CTAs take the pending ones' items
+        // one CTA per item: the running CTAs take the pending ones' items.
+        // When every CTA fits at once (2 per SM) there is nothing to take,
+        // and the CTAs skip the requests (a hint only: a CTA that starts
+        // late still runs its own item).
         const int grid = batch * a.Y * a.H_v * row_blocks(pa);
+        pa.steal = grid > 2 * (sms > 0 ? sms : 152) ? 1 : 0;
         if (launch_pdl(kern, dim3(grid), dim3(thr), Lp.total, stream, pa, grid) != cudaSuccess)
             return GDN_ERR_CUDA;
     } else {
         auto kern = gdn_verify_kernel<DK, BF16, TREE>;
-        static std::atomic<size_t> set{48 * 1024};
+        static SmemSet set;
         const Layout L = make_layout(a.T, DK, a.K);
         if (!ensure_smem(kern, L.total, set)) return GDN_ERR_CUDA;
         dim3 grid(nrb, a.H_v, batch * a.Y);
@@ -683,7 +710,7 @@ int launch_replay(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
     while (pa.rpi > kRowsPerWarp && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
     auto kern = a.K == 4 ? gdn_verify_persistent<DK, BF16, false, 4, kSlots, true>
                          : gdn_verify_persistent<DK, BF16, false, 0, kSlots, true>;
-    static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
+    static SmemSet set4, set0;
     if (!ensure_smem(kern, Lp.total, a.K == 4 ? set4 : set0)) return GDN_ERR_CUDA;
     const int grid = batch * a.Y * a.H_v * row_blocks(pa);
     return launch_pdl(kern, dim3(grid), dim3(threads), Lp.total, stream, pa, grid) == cudaSuccess ? GDN_OK
@@ -724,16 +751,26 @@ int check_common(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
 
 }  // namespace
 
+extern "C" int gdn_verify_span_ex(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
+                                  const void *b, const void *conv_w, const float *ssm_in,
+                                  const float *conv_in, float *ssm_ckpt, float *conv_ckpt, float *out,
+                                  int32_t *dev_status, uint32_t flags, gdn_stream_t stream) {
+    int rc = check_common(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out);
+    if (rc != GDN_OK) return rc;
+    if (flags & ~(uint32_t)GDN_VERIFY_STATE_READY) return GDN_ERR_FLAGS;
+    if (dev_status && !gdnhost::aligned_to(dev_status, 4)) return GDN_ERR_ALIGN;
+    VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out, nullptr,
+                             dev_status);
+    v.early = (flags & GDN_VERIFY_STATE_READY) ? 1 : 0;
+    return dispatch_verify<false>(d, v, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int gdn_verify_span(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
                                const void *b, const void *conv_w, const float *ssm_in,
                                const float *conv_in, float *ssm_ckpt, float *conv_ckpt, float *out,
                                int32_t *dev_status, gdn_stream_t stream) {
-    int rc = check_common(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out);
-    if (rc != GDN_OK) return rc;
-    if (dev_status && !gdnhost::aligned_to(dev_status, 4)) return GDN_ERR_ALIGN;
-    const VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt,
-                                   out, nullptr, dev_status);
-    return dispatch_verify<false>(d, v, static_cast<cudaStream_t>(stream));
+    return gdn_verify_span_ex(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out, dev_status,
+                              0u, stream);
 }
 
 extern "C" int gdn_tree_verify(const gdn_dims *d, int32_t n_nodes, const int32_t *parent_host,
@@ -741,6 +778,15 @@ extern "C" int gdn_tree_verify(const gdn_dims *d, int32_t n_nodes, const int32_t
                                const void *b, const void *conv_w, const float *ssm_in,
                                const float *conv_in, float *ssm_ckpt, float *conv_ckpt,
                                float *out, int32_t *dev_status, gdn_stream_t stream) {
+    return gdn_tree_verify_ex(d, n_nodes, parent_host, parent_dev, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt,
+                              conv_ckpt, out, dev_status, 0u, stream);
+}
+
+extern "C" int gdn_tree_verify_ex(const gdn_dims *d, int32_t n_nodes, const int32_t *parent_host,
+                                  const int32_t *parent_dev, const void *x, const void *a,
+                                  const void *b, const void *conv_w, const float *ssm_in,
+                                  const float *conv_in, float *ssm_ckpt, float *conv_ckpt,
+                                  float *out, int32_t *dev_status, uint32_t flags, gdn_stream_t stream) {
     if (!d) return GDN_ERR_NULL;
     if (n_nodes < 2) return GDN_ERR_TREE_TRUNCATED;
     int rc = check_common(d, n_nodes - 1, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out);
@@ -750,8 +796,10 @@ extern "C" int gdn_tree_verify(const gdn_dims *d, int32_t n_nodes, const int32_t
         return GDN_ERR_ALIGN;
     rc = gdnhost::check_tree(parent_host, d->batch, n_nodes, false, 0);
     if (rc != GDN_OK) return rc;
-    const VerifyArgs v = make_args(d, n_nodes - 1, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt,
-                                   conv_ckpt, out, parent_dev, dev_status);
+    if (flags & ~(uint32_t)GDN_VERIFY_STATE_READY) return GDN_ERR_FLAGS;
+    VerifyArgs v = make_args(d, n_nodes - 1, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out,
+                             parent_dev, dev_status);
+    v.early = (flags & GDN_VERIFY_STATE_READY) ? 1 : 0;
     return dispatch_verify<true>(d, v, static_cast<cudaStream_t>(stream));
 }
 
@@ -811,13 +859,13 @@ extern "C" int gdn_commit_replay(const gdn_dims *d, int32_t n_tok, const int32_t
     if (rc == 1) {  // the one-item-per-CTA replay kernel: inputs loaded directly
         if (d->d_k == 128) {
             auto kern = bf ? gdn_replay_kernel<128, true> : gdn_replay_kernel<128, false>;
-            static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
+            static SmemSet set_b, set_f;
             if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
             if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
                 return GDN_ERR_CUDA;
         } else {
             auto kern = bf ? gdn_replay_kernel<64, true> : gdn_replay_kernel<64, false>;
-            static std::atomic<size_t> set_b{48 * 1024}, set_f{48 * 1024};
+            static SmemSet set_b, set_f;
             if (!ensure_smem(kern, L.total, bf ? set_b : set_f)) return GDN_ERR_CUDA;
             if (launch_pdl(kern, grid, dim3(threads), L.total, st, v, accept_len_dev) != cudaSuccess)
                 return GDN_ERR_CUDA;

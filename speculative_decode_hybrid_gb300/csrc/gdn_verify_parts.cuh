@@ -39,6 +39,9 @@ struct VerifyArgs {
     float *ssm_out;         // replay commit: the live state, updated in place
     const int32_t *accept_len;  // replay commit: tokens to replay per request
     int rpi;                // value rows per work item: a multiple of 16, <= kRowsPerCta
+    int steal;              // work-stealing kernel: ask for pending items (0: every CTA runs its own item)
+    int early;              // GDN_VERIFY_STATE_READY: the state, conv taps / state and parents may be
+                            // read before the wait for the previous grid on the stream
 };
 
 // One work item: (request*layer by, value head h, row block rb).
@@ -228,40 +231,61 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
     }
 }
 
-// Per-head L2 norm of q and k, q scale, k.q; one warp per node.
+// L2 norms of one node's q and k, held by one warp: lane l holds elements
+// l, l + 32, ..., l + 32 (CPL - 1) of each. u / sqrt(sum u^2 + 1e-6) in place, q
+// also scaled by q_scale; returns k.q (the same value in every lane: each
+// xor-butterfly stage adds the same two operands in both partner lanes).
+// Every kernel normalises through this function, so the bytes of q and k
+// do not depend on which kernel computed them.
+template <int CPL>
+__device__ __forceinline__ float norm_node(float (&qv)[CPL], float (&kv)[CPL], float q_scale) {
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) {
+        sq = fmaf(qv[e], qv[e], sq);
+        sk = fmaf(kv[e], kv[e], sk);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+    }
+    // the hardware reciprocal square root (a few ulp), far inside the 2e-3
+    // tolerance of the states and outputs
+    const float iq = rsqrtf(sq + 1e-6f);
+    const float ik = rsqrtf(sk + 1e-6f);
+    float kq = 0.f;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) {
+        qv[e] = qv[e] * iq * q_scale;
+        kv[e] = kv[e] * ik;
+        kq = fmaf(qv[e], kv[e], kq);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    return kq;
+}
+
+// Per-head L2 norm of q and k (already convolved, in shared memory), q scale,
+// k.q; one warp per node.
 template <int DK>
 __device__ __forceinline__ void norm_qk(const VerifyArgs &p, float *q_s, float *k_s, float *kq_s, int count,
                                        int warp, int nwarps) {
-    constexpr int PER = DK / 32;
+    constexpr int CPL = DK / 32;
     const int lane = threadIdx.x & 31;
     for (int t = warp; t < count; t += nwarps) {
-        float qv[PER], kv[PER];
-        float sq = 0.f, sk = 0.f;
+        float qv[CPL], kv[CPL];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
+        for (int e = 0; e < CPL; ++e) {
             qv[e] = q_s[(size_t)t * DK + lane + 32 * e];
             kv[e] = k_s[(size_t)t * DK + lane + 32 * e];
-            sq = fmaf(qv[e], qv[e], sq);
-            sk = fmaf(kv[e], kv[e], sk);
         }
+        const float kq = norm_node<CPL>(qv, kv, p.q_scale);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, off);
-            sk += __shfl_xor_sync(0xffffffffu, sk, off);
-        }
-        const float iq = 1.0f / sqrtf(sq + 1e-6f);
-        const float ik = 1.0f / sqrtf(sk + 1e-6f);
-        float kq = 0.f;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            qv[e] = qv[e] * iq * p.q_scale;
-            kv[e] = kv[e] * ik;
+        for (int e = 0; e < CPL; ++e) {
             q_s[(size_t)t * DK + lane + 32 * e] = qv[e];
             k_s[(size_t)t * DK + lane + 32 * e] = kv[e];
-            kq = fmaf(qv[e], kv[e], kq);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
         if (lane == 0) kq_s[t] = kq;
     }
 }
@@ -286,10 +310,12 @@ __device__ __forceinline__ float conv_out(const float (&wr)[GDN_MAX_CONV_K], con
 // offset is a multiple of 16 bytes, see the host-side eligibility check).
 // with_qk false: the v range only (the q/k of the item are already on chip).
 // ntok: the tokens to copy (the first ntok of the span, ntok <= p.T).
+// parts: kStageX (the x tile), kStageTaps (conv taps and conv state) or both.
+constexpr int kStageX = 1, kStageTaps = 2, kStageAll = 3;
 template <int DK, bool BF16>
 __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I, unsigned char *xst,
                                               unsigned char *wst, unsigned char *cst, bool with_qk, int tid,
-                                              int nthreads, int ntok) {
+                                              int nthreads, int ntok, int parts = kStageAll) {
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int XS = 2 * DK + kRowsPerCta;
     const int T = p.T, K = p.K;
@@ -299,7 +325,7 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
     const size_t c_q = (size_t)I.g * DK, c_k = (size_t)p.H_k * DK + (size_t)I.g * DK;
     const size_t c_v = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;
     // x: per node, the three channel ranges [q | k | v]
-    {
+    if (parts & kStageX) {
         const int cq = DK * ES / 16, cv = I.R * ES / 16;
         const int r0 = with_qk ? 0 : 2 * cq, per_node = 2 * cq + cv - r0;
         for (int i = tid; i < ntok * per_node; i += nthreads) {
@@ -314,7 +340,7 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
         }
     }
     // conv taps [c][K] and conv state [c][K-1] of the three ranges
-    {
+    if (parts & kStageTaps) {
         const int wq = DK * K * ES / 16, wv = I.R * K * ES / 16, wn = 2 * wq + wv;
         for (int i = (with_qk ? 0 : 2 * wq) + tid; i < wn; i += nthreads) {
             size_t c0;
@@ -379,102 +405,224 @@ __host__ __device__ inline PipeLayout make_pipe_layout(int T, int DK, int K, int
     return L;
 }
 
-// conv1d + SiLU of item I from its staged inputs, by threads tid of nthreads.
-// Work unit = (channel, half of the nodes), consecutive threads on
-// consecutive channels (coalesced conv-checkpoint stores, conflict-free
-// staging reads). A chain keeps its K-window in registers (one staged load
-// per output); a tree gathers each node's window along its root path.
-// skip_qk: only the v channels (q and k are the previous item's, still in
-// shared memory; that item also wrote their conv checkpoints).
+// The K taps of local channel c from the staging buffer ([channel][K], bf16
+// or f32), widened to f32 (bf16 -> f32 is exact: the bits move to the high
+// half). With K = 4 one 8- or 16-byte load; consecutive channels in
+// consecutive lanes read consecutive words (no bank conflict).
+template <bool BF16, int KT, int KM>
+__device__ __forceinline__ void load_taps(const unsigned char *wst, int c, int K, float (&w)[KM]) {
+    if constexpr (KT == 4) {
+        if constexpr (BF16) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(wst + (size_t)c * 8);
+            w[0] = __uint_as_float(u.x << 16);
+            w[1] = __uint_as_float(u.x & 0xffff0000u);
+            w[2] = __uint_as_float(u.y << 16);
+            w[3] = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            const float4 f = *reinterpret_cast<const float4 *>(wst + (size_t)c * 16);
+            w[0] = f.x; w[1] = f.y; w[2] = f.z; w[3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < KM; ++j) w[j] = j < K ? ld_in<BF16>(wst, (size_t)c * K + j) : 0.f;
+    }
+}
+
+// conv1d + SiLU of item I from its staged inputs, fused with the q/k L2
+// norms: one warp per node. Lane l owns q and k channels l, l + 32, ... of
+// the key head (d_k / 32 each) and v channels l, l + 32, ... of the item, so
+// a node's sums of squares reduce inside its warp and q, k go to shared
+// memory once, normalised; consecutive lanes touch consecutive channels
+// (conflict-free staging reads, coalesced conv-checkpoint stores). Window position j of node t
+// comes from x row t - (K-1) + j of a chain (the conv state for negative
+// rows) or from the root-path table src_s of a tree. Each output is the
+// same fmaf chain over j = 0..K-1 as in the other kernels, so the bytes do
+// not depend on the kernel. The conv checkpoint after a node (window
+// positions 1..K-1, the last K-1 inputs) is written by the items that own
+// the channels: v, every item its own rows; q/k, when every CTA runs just
+// its own item (no work stealing, so no item skips the q/k conv), the
+// M = (value heads per key head) x (row blocks) items of the key head
+// share the 2 d_k / 32 channel groups (group hf * d_k/32 + e: channels
+// lane + 32 e of q (hf = 0) or k (hf = 1)) round robin, else the key head's
+// first item (never one that reuses q/k) writes them all.
+// skip_qk: only the v channels (q, k and k.q are the previous item's, still
+// in shared memory; that item also wrote their conv checkpoints).
 template <int DK, bool BF16, bool TREE, int KT>
-__device__ __forceinline__ void conv_staged(const VerifyArgs &p, const Item &I, const unsigned char *xst,
-                                            const unsigned char *wst, const unsigned char *cst,
-                                            const int *src_s, float *q_s, float *k_s, float *v_s,
-                                            bool skip_qk, int tid, int nthreads) {
+__device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item &I, const unsigned char *xst,
+                                                 const unsigned char *wst, const unsigned char *cst,
+                                                 const int *src_s, float *q_s, float *k_s, float *v_s,
+                                                 float *kq_s, bool skip_qk, int warp, int nwarps) {
     constexpr int XS = 2 * DK + kRowsPerCta;
+    constexpr int CPL = DK / 32;
     constexpr int KM = KT > 0 ? KT : GDN_MAX_CONV_K;
     const int T = p.T, K = KT > 0 ? KT : p.K;
+    const int lane = threadIdx.x & 31;
     const float *cstf = reinterpret_cast<const float *>(cst);
     const size_t cc_tok = (size_t)p.C * (K - 1);
-    {
-        const int lc0 = skip_qk ? 2 * DK : 0, nch = 2 * DK + I.R - lc0;
-        const bool own_qk = (I.h % (p.H_v / p.H_k) == 0) && I.rb == 0;
-        const int nchunk = T >= 8 ? 2 : 1;
-        const int tc = (T + nchunk - 1) / nchunk;
-        for (int u = tid; u < nch * nchunk; u += nthreads) {
-            const int lc = lc0 + u % nch, tb = (u / nch) * tc, te = min(T, tb + tc);
-            float *dst = lc < DK ? q_s + lc : lc < 2 * DK ? k_s + (lc - DK) : v_s + (lc - 2 * DK);
-            const int stride = lc < 2 * DK ? DK : kRowsPerCta;
-            const bool own = (lc >= 2 * DK || own_qk) && p.conv_ckpt != nullptr;
-            float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)item_channel<DK>(p, I, lc) * (K - 1);
-            float wr[KM];
+    const bool ckpt = p.conv_ckpt != nullptr;
+    // q/k channel groups whose conv checkpoints this item writes (bit hf * CPL + e)
+    unsigned qk_own = 0;
+    if (ckpt && !skip_qk) {
+        const int G = p.H_v / p.H_k, nrb = row_blocks(p);
+        if (p.steal == 0) {
+            const int M = G * nrb, m = (I.h % G) * nrb + I.rb;
+            for (int gr = m; gr < 2 * CPL; gr += M) qk_own |= 1u << gr;
+        } else if (I.h % G == 0 && I.rb == 0) {
+            qk_own = (1u << (2 * CPL)) - 1u;
+        }
+    }
+    float *cck = ckpt ? p.conv_ckpt + (size_t)I.by * T * cc_tok : nullptr;
+    const size_t gq = (size_t)I.g * DK + lane;            // global q channel of this lane's element 0
+    const size_t gk = (size_t)p.H_k * DK + gq;            // and k channel
+    const size_t gv = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;  // global channel of v row 0
+    for (int t = warp; t < T; t += nwarps) {
+        // window position j: x row src[j] >= 0, or conv-state slot -1 - src[j]
+        int src[KM];
 #pragma unroll
-            for (int j = 0; j < KM; ++j) wr[j] = j < K ? ld_in<BF16>(wst, (size_t)lc * K + j) : 0.f;
-            if constexpr (!TREE) {
-                // win[j], j < K-1: sequence position tb-(K-1)+j (x row when >= 0,
-                // else conv-state slot K-1+position)
-                float win[KM];
-#pragma unroll
-                for (int j = 0; j < KM; ++j) {
-                    win[j] = 0.f;
-                    if (j < K - 1) {
-                        const int sp = tb - (K - 1) + j;
-                        win[j] = sp >= 0 ? ld_in<BF16>(xst, (size_t)sp * XS + lc)
-                                         : cstf[(size_t)lc * (K - 1) + (K - 1 + sp)];
-                    }
-                }
-                for (int t = tb; t < te; ++t) {
-                    const float xv = ld_in<BF16>(xst, (size_t)t * XS + lc);
-                    float acc = 0.f;
-#pragma unroll
-                    for (int j = 0; j < KM; ++j)
-                        if (j < K) acc = fmaf(wr[j], j < K - 1 ? win[j] : xv, acc);
-                    dst[(size_t)t * stride] = silu(acc);
-#pragma unroll
-                    for (int j = 0; j < KM - 1; ++j) {
-                        if (j < K - 2) win[j] = win[j + 1];
-                        else if (j == K - 2) win[j] = xv;
-                    }
-                    if (own) {
-#pragma unroll
-                        for (int j = 0; j < KM - 1; ++j)
-                            if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j];
-                    }
-                }
-            } else {
-                for (int t = tb; t < te; ++t) {
-                    float win[KM];
-                    float acc = 0.f;
-#pragma unroll
-                    for (int j = 0; j < KM; ++j) {
-                        win[j] = 0.f;
-                        if (j < K) {
-                            const int sn = src_s[t * K + j];  // >= 1: node; else -1 - conv-state slot
-                            win[j] = sn >= 1 ? ld_in<BF16>(xst, (size_t)(sn - 1) * XS + lc)
-                                             : cstf[(size_t)lc * (K - 1) + (-1 - sn)];
-                            acc = fmaf(wr[j], win[j], acc);
-                        }
-                    }
-                    dst[(size_t)t * stride] = silu(acc);
-                    if (own) {
-#pragma unroll
-                        for (int j = 0; j < KM - 1; ++j)
-                            if (j < K - 1) cck[(size_t)t * cc_tok + j] = win[j + 1];
-                    }
+        for (int j = 0; j < KM; ++j) {
+            int s = 0;
+            if (j < K) {
+                if constexpr (TREE) {
+                    const int sn = src_s[t * K + j];  // >= 1: node; else -1 - slot
+                    s = sn >= 1 ? sn - 1 : sn;
+                } else {
+                    const int sp = t - (K - 1) + j;
+                    s = sp >= 0 ? sp : -1 - (K - 1 + sp);
                 }
             }
+            src[j] = s;
+        }
+        if (!skip_qk) {
+            // q (half 0) and k (half 1): element e is channel lane + 32 e
+            float acc[2][CPL];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int e = 0; e < CPL; ++e) {
+                    const int c = hf * DK + lane + 32 * e;  // local channel
+                    float w[KM];
+                    load_taps<BF16, KT, KM>(wst, c, K, w);
+                    float *cc = (qk_own >> (hf * CPL + e)) & 1u
+                                    ? cck + (size_t)t * cc_tok + ((hf ? gk : gq) + 32 * e) * (K - 1)
+                                    : nullptr;
+                    float a = 0.f;
+#pragma unroll
+                    for (int j = 0; j < KM; ++j) {
+                        if (j < K) {
+                            const float xv = src[j] >= 0 ? ld_in<BF16>(xst, (size_t)src[j] * XS + c)
+                                                         : cstf[(size_t)c * (K - 1) + (-1 - src[j])];
+                            a = fmaf(w[j], xv, a);
+                            if (cc && j >= 1) cc[j - 1] = xv;
+                        }
+                    }
+                    acc[hf][e] = silu(a);
+                }
+            }
+            const float kq = norm_node<CPL>(acc[0], acc[1], p.q_scale);
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) {
+                q_s[(size_t)t * DK + lane + 32 * e] = acc[0][e];
+                k_s[(size_t)t * DK + lane + 32 * e] = acc[1][e];
+            }
+            if (lane == 0) kq_s[t] = kq;
+        }
+        for (int lc = lane; lc < I.R; lc += 32) {
+            const int c = 2 * DK + lc;
+            float w[KM];
+            load_taps<BF16, KT, KM>(wst, c, K, w);
+            float *cv = ckpt ? cck + (size_t)t * cc_tok + (gv + lc) * (K - 1) : nullptr;
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < KM; ++j) {
+                if (j < K) {
+                    const float xv = src[j] >= 0 ? ld_in<BF16>(xst, (size_t)src[j] * XS + c)
+                                                 : cstf[(size_t)c * (K - 1) + (-1 - src[j])];
+                    acc = fmaf(w[j], xv, acc);
+                    if (cv && j >= 1) cv[j - 1] = xv;
+                }
+            }
+            v_s[(size_t)t * kRowsPerCta + lc] = silu(acc);
         }
     }
 }
 
-// Raise a kernel's dynamic shared-memory limit once per size (per process;
-// raising it again is harmless).
+// Fill L2 with the 128-byte lines of [base, base + bytes), the lines spread
+// over the group's threads. A prefetch only fills L2, the point of
+// coherence, and has no effect on what any load later returns.
+__device__ __forceinline__ void prefetch_l2_range(const void *base, size_t bytes, int tid, int nthreads) {
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(base) + bytes;
+    for (uintptr_t a = (reinterpret_cast<uintptr_t>(base) & ~uintptr_t(127)) + (uintptr_t)tid * 128u; a < a1;
+         a += (uintptr_t)nthreads * 128u)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+// Warm L2 with item I's inputs: its state rows, x tile (all p.T nodes), conv
+// taps and conv state, gates and (tree) parents. Called before the kernel
+// waits for the previous grid on the stream: that grid may still be writing
+// some of these bytes, which is harmless for a prefetch, and the real loads
+// after the wait then hit L2 instead of DRAM.
+// with_state false: only the x tile, gates and parents (the rest is being
+// loaded already).
+template <int DK, bool BF16, bool TREE>
+__device__ __forceinline__ void prefetch_l2_item(const VerifyArgs &p, const Item &I, int tid, int nthreads,
+                                                 bool with_state = true) {
+    constexpr int ES = BF16 ? 2 : 4;
+    const int T = p.T, K = p.K;
+    const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
+    if (with_state) prefetch_l2_range(p.ssm_in + head_off, (size_t)I.R * DK * 4, tid, nthreads);
+    const size_t c_q = (size_t)I.g * DK, c_k = (size_t)p.H_k * DK + c_q;
+    const size_t c_v = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;
+    const unsigned char *xg = static_cast<const unsigned char *>(p.x);
+    for (int i = tid; i < 3 * T; i += nthreads) {  // (node, channel range) pairs
+        const int t = i / 3, r = i - 3 * t;
+        const size_t c0 = r == 0 ? c_q : r == 1 ? c_k : c_v;
+        prefetch_l2_range(xg + (((size_t)I.by * T + t) * p.C + c0) * ES, (r < 2 ? DK : I.R) * (size_t)ES, 0, 1);
+    }
+    const unsigned char *wg = static_cast<const unsigned char *>(p.w);
+    const int sub = tid & 31, lanes = 32;  // small ranges: one warp each
+    const int w = tid >> 5;
+    const int nw = nthreads >> 5;
+    for (int r = w; with_state && r < 6; r += nw) {
+        const size_t c0 = (r % 3) == 0 ? c_q : (r % 3) == 1 ? c_k : c_v;
+        const size_t n = (r % 3) == 2 ? (size_t)I.R : (size_t)DK;
+        if (r < 3)
+            prefetch_l2_range(wg + ((size_t)I.y * p.C + c0) * K * ES, n * K * ES, sub, lanes);
+        else if (p.conv_in && K > 1)
+            prefetch_l2_range(p.conv_in + ((size_t)I.by * p.C + c0) * (K - 1), n * (K - 1) * 4, sub, lanes);
+    }
+    if (tid < T) {
+        const size_t gi = ((size_t)I.by * T + tid) * p.H_v + I.h;
+        prefetch_l2_range(static_cast<const unsigned char *>(p.a) + gi * ES, ES, 0, 1);
+        prefetch_l2_range(static_cast<const unsigned char *>(p.b) + gi * ES, ES, 0, 1);
+    }
+    if constexpr (TREE) {
+        if (tid == 0) prefetch_l2_range(p.parent + (size_t)I.bidx * (T + 1), (size_t)(T + 1) * 4, 0, 1);
+    }
+}
+
+// The dynamic shared-memory limit one kernel has been raised to, per device:
+// cudaFuncSetAttribute applies to the current device only, so a process that
+// drives several GPUs must raise it on each of them.
+constexpr int kSmemDevices = 64;
+struct SmemSet {
+    std::atomic<size_t> v[kSmemDevices];
+    SmemSet() {
+        for (auto &x : v) x.store(48 * 1024, std::memory_order_relaxed);
+    }
+};
+
+// Raise a kernel's dynamic shared-memory limit on the current device once per
+// size (raising it again is harmless; devices beyond the cache raise it on
+// every call).
 template <typename K>
-bool ensure_smem(K kern, size_t smem, std::atomic<size_t> &set) {
-    if (smem <= set.load(std::memory_order_relaxed)) return true;
+bool ensure_smem(K kern, size_t smem, SmemSet &set) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+    const bool cached = dev < kSmemDevices;
+    if (cached && smem <= set.v[dev].load(std::memory_order_relaxed)) return true;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return false;
-    set.store(smem, std::memory_order_relaxed);
+    if (cached) set.v[dev].store(smem, std::memory_order_relaxed);
     return true;
 }
 
@@ -504,6 +652,8 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
     v.ssm_out = nullptr;
     v.accept_len = nullptr;
     v.rpi = kRowsPerCta;
+    v.steal = 1;
+    v.early = 0;
     return v;
 }
 

@@ -188,9 +188,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     {
         VerifyArgs pc = p;  // the commit only needs its first Te tokens
         pc.T = Te;
-        conv_staged<DK, BF16, false, KT>(pc, I, xst, wst, cst, nullptr, q_s, k_s, v_s, false, tid, nthreads);
-        __syncthreads();
-        norm_qk<DK>(pc, q_s, k_s, kq_s, Te, tid >> 5, nthreads >> 5);
+        conv_norm_staged<DK, BF16, false, KT>(pc, I, xst, wst, cst, nullptr, q_s, k_s, v_s, kq_s, false, tid >> 5,
+                                              nthreads >> 5);
     }
     __syncthreads();  // q, k normalised; the staging buffers are free
 
@@ -462,7 +461,7 @@ int launch_wy(const VerifyArgs &a, int batch, const int32_t *accept_len, cudaStr
     const WyLayout L = make_wy_layout(a.T, DK, a.K, BF16 ? 2 : 4);
     if (L.total > kMaxSmem) return GDN_ERR_DIMS;
     auto kern = a.K == 4 ? gdn_wy_kernel<DK, BF16, 4, COMMIT> : gdn_wy_kernel<DK, BF16, 0, COMMIT>;
-    static std::atomic<size_t> set4{48 * 1024}, set0{48 * 1024};
+    static SmemSet set4, set0;
     if (!ensure_smem(kern, L.total, a.K == 4 ? set4 : set0)) return GDN_ERR_CUDA;
     return launch_pdl(kern, dim3((unsigned)n_items), dim3(kThreads), L.total, st, a, accept_len) == cudaSuccess
                ? GDN_OK

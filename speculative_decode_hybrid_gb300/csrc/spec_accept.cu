@@ -240,23 +240,30 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_accept_scratch[GDN_STATIC_SCRATCH_BYTES];
 
-// Device address of g_accept_scratch, looked up once per device. In host
-// code the symbol itself is only a host-side stand-in, never a device
-// address, so kernels must be given the looked-up pointer.
+// Device address of g_accept_scratch, looked up per device. In host code the
+// symbol itself is only a host-side stand-in, never a device address, so
+// kernels must be given the looked-up pointer. Only a successful lookup is
+// kept: a failed one (for example a first call made during a stream capture
+// that forbids it) fails that call alone, and the next call tries again.
+// The kept address belongs to the device's current context; after a
+// cudaDeviceReset the array lives elsewhere, which this cache does not
+// follow (the entry point does not support cudaDeviceReset).
 constexpr int kMaxDevices = 64;
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
 
 int static_scratch(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
-    std::call_once(g_scratch_once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
         void *p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_accept_scratch);
-        g_scratch_ptr[dev] = g_scratch_err[dev] == cudaSuccess ? p : nullptr;
-    });
-    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return GDN_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();  // leave no sticky launch error behind for the next call
+            return GDN_ERR_CUDA;
+        }
+        g_scratch_ptr[dev] = p;
+    }
     *out = g_scratch_ptr[dev];
     return GDN_OK;
 }

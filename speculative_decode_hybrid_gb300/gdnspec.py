@@ -31,6 +31,9 @@ GDN_ERR_TREE_TRUNCATED = 8
 GDN_ERR_TREE_NOT_CHAIN = 9
 GDN_ERR_WORKSPACE = 10
 GDN_ERR_CUDA = 11
+GDN_ERR_FLAGS = 12
+
+GDN_VERIFY_STATE_READY = 0x1
 
 GDN_DEV_TOKEN_RANGE = 0x1
 GDN_DEV_NAN_LOGIT = 0x2
@@ -46,7 +49,8 @@ GDN_WY_MAX_TOKENS = 16
 EXPORTED = ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
             "spec_accept_workspace_bytes", "gdn_rollback_restore", "gdn_tree_check",
             "gdn_status_str", "gdn_verify_span_nockpt", "gdn_commit_replay", "spec_topk",
-            "spec_topk_workspace_bytes", "gdn_verify_span_wy", "gdn_commit_wy")
+            "spec_topk_workspace_bytes", "gdn_verify_span_wy", "gdn_commit_wy", "gdn_verify_span_ex",
+            "gdn_tree_verify_ex")
 
 
 class GdnError(RuntimeError):
@@ -89,6 +93,9 @@ def load(path: Optional[str] = None):
         dp = ctypes.POINTER(gdn_dims)
         lib.gdn_verify_span.argtypes = [dp, i32] + [vp] * 9 + [vp, vp]
         lib.gdn_tree_verify.argtypes = [dp, i32, vp, vp] + [vp] * 9 + [vp, vp]
+        u32 = ctypes.c_uint32
+        lib.gdn_verify_span_ex.argtypes = [dp, i32] + [vp] * 9 + [vp, u32, vp]
+        lib.gdn_tree_verify_ex.argtypes = [dp, i32, vp, vp] + [vp] * 9 + [vp, u32, vp]
         lib.spec_accept_greedy.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         lib.spec_accept_workspace_bytes.argtypes = [i32, i32]
         lib.spec_accept_workspace_bytes.restype = sz
@@ -103,7 +110,8 @@ def load(path: Optional[str] = None):
         lib.gdn_tree_check.argtypes = [vp, i32, i32, i32, i32]
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
-        for f in ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
+        for f in ("gdn_verify_span", "gdn_tree_verify", "gdn_verify_span_ex", "gdn_tree_verify_ex",
+                  "spec_accept_greedy",
                   "gdn_rollback_restore", "gdn_tree_check", "gdn_verify_span_nockpt",
                   "gdn_commit_replay", "spec_topk", "gdn_verify_span_wy", "gdn_commit_wy"):
             getattr(lib, f).restype = ctypes.c_int
@@ -146,24 +154,30 @@ def _ok(rc: int, what: str):
 
 
 def gdn_verify_span(dims: gdn_dims, n_tok: int, x, a, b, conv_w, ssm_in, conv_in,
-                    ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None) -> None:
-    rc = load().gdn_verify_span(ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b), _ptr(conv_w),
-                                _ptr(ssm_in), _ptr(conv_in), _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out),
-                                _ptr(dev_status), _stream(stream))
-    _ok(rc, "gdn_verify_span")
+                    ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None, flags: int = 0) -> None:
+    """gdn_verify_span, or gdn_verify_span_ex when flags (GDN_VERIFY_*) are given."""
+    args = (ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b), _ptr(conv_w), _ptr(ssm_in),
+            _ptr(conv_in), _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out), _ptr(dev_status))
+    if flags:
+        _ok(load().gdn_verify_span_ex(*args, int(flags), _stream(stream)), "gdn_verify_span_ex")
+    else:
+        _ok(load().gdn_verify_span(*args, _stream(stream)), "gdn_verify_span")
 
 
 def gdn_tree_verify(dims: gdn_dims, n_nodes: int, parent_host, parent_dev, x, a, b, conv_w, ssm_in,
-                    conv_in, ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None) -> None:
+                    conv_in, ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None, flags: int = 0) -> None:
+    """gdn_tree_verify, or gdn_tree_verify_ex when flags (GDN_VERIFY_*) are given."""
     import numpy as np
     ph = None
     if parent_host is not None:
         ph = np.ascontiguousarray(parent_host, dtype=np.int32)
-    rc = load().gdn_tree_verify(ctypes.byref(dims), int(n_nodes), _ptr(ph), _ptr(parent_dev), _ptr(x),
-                                _ptr(a), _ptr(b), _ptr(conv_w), _ptr(ssm_in), _ptr(conv_in),
-                                _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out), _ptr(dev_status),
-                                _stream(stream))
-    _ok(rc, "gdn_tree_verify")
+    args = (ctypes.byref(dims), int(n_nodes), _ptr(ph), _ptr(parent_dev), _ptr(x), _ptr(a), _ptr(b),
+            _ptr(conv_w), _ptr(ssm_in), _ptr(conv_in), _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out),
+            _ptr(dev_status))
+    if flags:
+        _ok(load().gdn_tree_verify_ex(*args, int(flags), _stream(stream)), "gdn_tree_verify_ex")
+    else:
+        _ok(load().gdn_tree_verify(*args, _stream(stream)), "gdn_tree_verify")
 
 
 def spec_accept_workspace_bytes(batch: int, n_nodes: int) -> int:

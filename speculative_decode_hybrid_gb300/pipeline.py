@@ -143,12 +143,13 @@ class SpecStep:
                                           q_scale=self.dims.q_scale)
         return cache[(nb, ny)]
 
-    def verify_block(self, b0: int, b1: int, y0: int, y1: int, kind: str = "checkpoint", stream=None):
+    def verify_block(self, b0: int, b1: int, y0: int, y1: int, kind: str = "checkpoint", stream=None,
+                     flags: int = 0):
         """The verify of requests [b0, b1) x layers [y0, y1) as one launch.
         The slices of the [B][Y] layouts must be contiguous: all layers, or
         one request. kind: "checkpoint", "replay" (no checkpoints: the
         faster form, as verify_nockpt_fastest) or "wy" (no checkpoints,
-        chunked form)."""
+        chunked form). flags: GDN_VERIFY_* of the checkpoint verify."""
         s = self.shape
         if not (y0 == 0 and y1 == s.layers) and b1 - b0 != 1:
             raise ValueError("a layer range is contiguous for one request only")
@@ -162,10 +163,11 @@ class SpecStep:
             if self.tree:
                 G.gdn_tree_verify(d, self.n_nodes, self.parent_host[bs], self.parent[bs], x, a, b, w, S, Cs,
                                   self.ssm_ckpt[bs, ys], self.conv_ckpt[bs, ys], self.out[bs, ys],
-                                  self.dev_status, stream)
+                                  self.dev_status, stream, flags=flags)
             else:
                 G.gdn_verify_span(d, self.n_tok, x, a, b, w, S, Cs, self.ssm_ckpt[bs, ys],
-                                  self.conv_ckpt[bs, ys], self.out[bs, ys], self.dev_status, stream)
+                                  self.conv_ckpt[bs, ys], self.out[bs, ys], self.dev_status, stream,
+                                  flags=flags)
         elif kind == "replay" and self.n_tok > G.GDN_WY_MAX_TOKENS:
             G.gdn_verify_span_nockpt(d, self.n_tok, x, a, b, w, S, Cs, self.out[bs, ys], self.dev_status, stream)
         else:
@@ -194,13 +196,18 @@ class SpecStep:
         return [(a, b, 0, Y) for a, b in spans]
 
     # -- per-layer launches: how a model whose layers run in sequence calls it
-    def verify_per_layer(self, stream=None):
+    def verify_per_layer(self, stream=None, state_ready: bool = True):
         """The verify of each layer as its own launch (batch 1, where a
-        layer's slices of the [B][Y] layouts are contiguous)."""
+        layer's slices of the [B][Y] layouts are contiguous). Every launch
+        after the first follows the previous layer's verify, which writes
+        none of its state, conv taps or parents, so it carries
+        GDN_VERIFY_STATE_READY (state_ready=False: no flags). The first one
+        follows whatever came before (a restore writes the live state)."""
         if self.shape.batch != 1:
             raise ValueError("per-layer launches are laid out for batch 1")
         for y in range(self.shape.layers):
-            self.verify_block(0, 1, y, y + 1, "checkpoint", stream)
+            fl = G.GDN_VERIFY_STATE_READY if state_ready and y > 0 else 0
+            self.verify_block(0, 1, y, y + 1, "checkpoint", stream, flags=fl)
 
     def step_per_layer(self, stream=None):
         """verify (one launch per layer) -> accept -> restore (all layers)."""

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, 12):
+    for code in range(0, 13):
         s = G.status_str(code)
         assert s and s != "unknown status", code
     assert G.status_str(999) == "unknown status"
@@ -219,3 +219,22 @@ def test_topk_validation(lib):
     assert f(4, 100, 8, None, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_NULL
     assert f(4, 100, 8, FAKE + 4, FAKE, FAKE, FAKE, ws, None, None) == G.GDN_ERR_ALIGN
     assert f(4, 100, 8, FAKE, FAKE, FAKE, FAKE, ws - 8, None, None) == G.GDN_ERR_WORKSPACE
+
+
+def test_verify_ex_validates_flags_before_launch(lib):
+    """The flagged entry points check everything gdn_verify_span /
+    gdn_tree_verify check, and reject flag bits the library does not define
+    (GDN_ERR_FLAGS) before anything is queued."""
+    d = _dims()
+    args = [FAKE] * 9
+    assert lib.gdn_verify_span_ex(ctypes.byref(d), 4, *args, None, 0x2, None) == G.GDN_ERR_FLAGS
+    assert lib.gdn_verify_span_ex(ctypes.byref(d), 4, *args, None, 0x80000000, None) == G.GDN_ERR_FLAGS
+    assert lib.gdn_verify_span_ex(ctypes.byref(d), 0, *args, None, G.GDN_VERIFY_STATE_READY, None) == \
+        G.GDN_ERR_DIMS
+    assert lib.gdn_verify_span_ex(None, 4, *args, None, 0, None) == G.GDN_ERR_NULL
+    par = np.array([-1, 0, 1, 1], dtype=np.int32)
+    assert lib.gdn_tree_verify_ex(ctypes.byref(d), 4, par.ctypes.data, *args, FAKE, None, 0x4, None) == \
+        G.GDN_ERR_FLAGS
+    bad = np.array([-1, 0, 3, 1], dtype=np.int32)
+    assert lib.gdn_tree_verify_ex(ctypes.byref(d), 4, bad.ctypes.data, *args, FAKE, None,
+                                  G.GDN_VERIFY_STATE_READY, None) == G.GDN_ERR_TREE_PARENT

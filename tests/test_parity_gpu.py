@@ -72,19 +72,24 @@ def test_workload3_tree_full_size_all_layers():
     assert int(kl[0]) == int(depth[int(kn[0])])
 
 
-def test_workload4_batched_full_size_sampled():
-    """16 requests x 48 layers (25 GiB of checkpoints): acceptance and restore
-    of every request; checkpoints of sampled (request, layer) pairs."""
+def test_workload4_batched_full_size_every_request():
+    """16 requests x 48 layers (25 GiB of checkpoints): acceptance of every
+    request; checkpoints, outputs and restored state of every request against
+    the oracle on two layers each (different layers for different requests,
+    so the 32 pairs cover the first, middle and last layers); restored bytes
+    of every request against its own slot on three layers."""
     wl = W.make_workload(4, seed=4)
     st = run(wl)
     kl, kn = check_accept_vs_oracle(st, wl)
-    pairs = [(0, 0), (3, 11), (7, 23), (12, 40), (15, 47)]
+    s = wl.shape
+    pairs = [(r, y) for r in range(s.batch) for y in sorted({(3 * r) % s.layers, (s.layers - 1 - 3 * r) % s.layers})]
+    assert len(pairs) == 2 * s.batch
+    assert {y for _, y in pairs} >= {0, s.layers - 1}
     refs = {}
     for r, y in pairs:
         refs[(r, y)] = oracle.verify_request(wl, r, layers=[y])[0]
         check_layer_vs_oracle(st, wl, r, y, refs[(r, y)])
-    # restored bytes of every request on sampled layers
-    for r in range(wl.shape.batch):
+    for r in range(s.batch):
         node = int(kn[r])
         for y in (0, 29, 47):
             g = st.ssm_state[r, y].cpu().numpy()
@@ -92,7 +97,9 @@ def test_workload4_batched_full_size_sampled():
             np.testing.assert_array_equal(g, want)
     for (r, y), (ck, cc, _) in refs.items():
         want = oracle.restore(ck, int(kn[r]), wl.ssm0[r, y])
-        assert slice_rel_err(st.ssm_state[r, y].cpu().numpy(), want, 128 * 128) <= TOL
+        assert slice_rel_err(st.ssm_state[r, y].cpu().numpy(), want, s.d_v * s.d_k) <= TOL
+        want_c = oracle.restore(cc, int(kn[r]), wl.conv0[r, y])
+        np.testing.assert_array_equal(st.conv_state[r, y].cpu().numpy(), want_c.astype(np.float32))
     assert int(st.dev_status.item()) == 0
     assert len(set(int(k) for k in kl)) > 1  # independent acceptance per request
 
@@ -696,3 +703,38 @@ def test_per_layer_launches_equal_one_launch(tree):
     assert torch.equal(a.out, b.out)
     assert torch.equal(a.ssm_ckpt, b.ssm_ckpt) and torch.equal(a.conv_ckpt, b.conv_ckpt)
     assert int(b.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_state_ready_flag_per_layer(tree):
+    """GDN_VERIFY_STATE_READY (the state, conv taps, conv state and parents
+    read before the wait for the previous launch): per-layer launches with
+    the flag give the bytes of the same launches without it and match the
+    oracle; and three graph replays of the whole step (flagged per-layer
+    verify -> accept -> restore, where each restore rewrites the state the
+    next replay reads) leave the state of three eager unflagged steps."""
+    wl = W.make_workload(3 if tree else 2, seed=21, layers=6)
+    a, b = SpecStep(wl), SpecStep(wl)
+    a.verify_per_layer(state_ready=False)
+    b.verify_per_layer()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out, b.out)
+    assert torch.equal(a.ssm_ckpt, b.ssm_ckpt) and torch.equal(a.conv_ckpt, b.conv_ckpt)
+    for y in (0, 3, 5):
+        check_layer_vs_oracle(b, wl, 0, y)
+    assert int(b.dev_status.item()) == 0
+
+    a2, b2 = SpecStep(wl), SpecStep(wl)
+    b2.capture("checkpoint-per-layer")  # runs one eager step first
+    for _ in range(2):
+        b2.replay()
+    for _ in range(3):
+        a2.verify_per_layer(state_ready=False)
+        a2.accept()
+        a2.restore()
+    torch.cuda.synchronize()
+    if int(a2.accept_node[0]) > 0:  # the state moved: the later steps read restored state
+        assert not torch.equal(a2.ssm_state, SpecStep(wl).ssm_state)
+    assert torch.equal(a2.ssm_state, b2.ssm_state) and torch.equal(a2.conv_state, b2.conv_state)
+    assert torch.equal(a2.ssm_ckpt, b2.ssm_ckpt) and torch.equal(a2.out, b2.out)
+    assert int(b2.dev_status.item()) == 0
