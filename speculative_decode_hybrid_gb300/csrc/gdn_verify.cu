@@ -87,20 +87,23 @@ __device__ __forceinline__ void load_rows(RowState<DK, SL> &rs, const float *src
     }
 }
 
-// Trees park each thread's initial rows in tensor memory (its own lane;
-// warps 4..7 use the columns after those of warps 0..3), so that the root's
-// later children restart from there instead of from DRAM. Warp-collective.
+// Trees park the state of a branch point (the initial rows, or a node with
+// children still to run) in tensor memory, so that its later children
+// restart from there instead of from its checkpoint. Slot k of a thread's
+// rows: its own lane, columns from 2 k kWords (warps 4..7 after those of
+// warps 0..3). Warp-collective.
 template <int DK, int SL>
-__device__ __forceinline__ unsigned park_addr(unsigned tmem) {
+__device__ __forceinline__ unsigned park_addr(unsigned tmem, int slot) {
     const int warp = threadIdx.x >> 5;
-    return tmem + ((unsigned)(32 * (warp & 3)) << 16) + (unsigned)((warp >> 2) * RowState<DK, SL>::kWords);
+    constexpr int W = RowState<DK, SL>::kWords;
+    return tmem + ((unsigned)(32 * (warp & 3)) << 16) + (unsigned)((2 * slot + (warp >> 2)) * W);
 }
 
 template <int DK, int SL>
-__device__ __forceinline__ void park_rows(const RowState<DK, SL> &rs, unsigned tmem) {
+__device__ __forceinline__ void park_rows(const RowState<DK, SL> &rs, unsigned tmem, int slot) {
     constexpr int NV4 = RowState<DK, SL>::NV4;
     static_assert((SL * NV4) % 2 == 0, "8 words per tensor-memory store");
-    const unsigned base = park_addr<DK, SL>(tmem);
+    const unsigned base = park_addr<DK, SL>(tmem, slot);
 #pragma unroll
     for (int k = 0; k < SL * NV4; k += 2) {
         const float4 x = rs.S[k / NV4][k % NV4], y = rs.S[(k + 1) / NV4][(k + 1) % NV4];
@@ -112,9 +115,9 @@ __device__ __forceinline__ void park_rows(const RowState<DK, SL> &rs, unsigned t
 }
 
 template <int DK, int SL>
-__device__ __forceinline__ void fetch_rows(RowState<DK, SL> &rs, unsigned tmem) {
+__device__ __forceinline__ void fetch_rows(RowState<DK, SL> &rs, unsigned tmem, int slot) {
     constexpr int NV4 = RowState<DK, SL>::NV4;
-    const unsigned base = park_addr<DK, SL>(tmem);
+    const unsigned base = park_addr<DK, SL>(tmem, slot);
 #pragma unroll
     for (int k = 0; k < SL * NV4; k += 2) {
         unsigned v[8];
@@ -127,35 +130,18 @@ __device__ __forceinline__ void fetch_rows(RowState<DK, SL> &rs, unsigned tmem) 
     }
 }
 
-// One node t of the recurrence for this thread's rows: one checkpoint slot.
-// s_in: the item's initial rows; ck0: slot 0 of the item's rows.
-// `prev` is the node whose state the registers hold (0: the initial state).
-// PARK: the initial rows are parked in tensor memory at `tmem` (trees).
-template <int DK, bool TREE, int SL, bool PARK = false>
-__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK, SL> &rs, int t, int prev,
-                                               const float *s_in, float *ck0, const float *q_s,
-                                               const float *k_s, const float *v_s, float *o_s,
-                                               const float *a_s, const float *b_s, const float *kq_s,
-                                               const int *par_s, unsigned tmem = 0) {
+// One node t of the recurrence for this thread's rows (whose registers hold
+// the state of the node's parent): one checkpoint slot.
+// ck0: slot 0 of the item's rows.
+template <int DK, int SL>
+__device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK, SL> &rs, int t, float *ck0,
+                                               const float *q_s, const float *k_s, const float *v_s,
+                                               float *o_s, const float *a_s, const float *b_s,
+                                               const float *kq_s) {
     constexpr int NV4 = RowState<DK, SL>::NV4;
     const int lane = threadIdx.x & 31;
     const int j8 = lane & (kLanesPerRow - 1);
     const size_t slot = (size_t)p.H_v * p.d_v * DK;
-    if constexpr (TREE) {
-        const int pp = par_s[t + 1];
-        if (pp != prev) {
-            if (PARK && pp == 0) {
-                fetch_rows(rs, tmem);
-            } else {
-                const float *src = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
-#pragma unroll
-                for (int s = 0; s < SL; ++s)
-#pragma unroll
-                    for (int m = 0; m < NV4; ++m)
-                        rs.S[s][m] = ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
-            }
-        }
-    }
     float4 kk[NV4], qq[NV4];
 #pragma unroll
     for (int m = 0; m < NV4; ++m) {
@@ -201,7 +187,13 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
     }
 }
 
-// The recurrence over all nodes of one item.
+// The recurrence over all nodes of one item. Trees run the nodes in the
+// depth-first order of the tree tables and follow their reload plan: a
+// node whose parent is not the node just computed takes the parent's state
+// from its tensor-memory slot (PARK, the plan's slots were sized for
+// `tmem`), or from its checkpoint (the same thread wrote those addresses:
+// program order makes them visible), or from the initial rows; a branch
+// point is parked after its step.
 template <int DK, bool TREE, int SL, bool PARK = false>
 __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL> &rs, const float *s_in,
                                           float *ck0, const float *q_s, const float *k_s,
@@ -209,18 +201,36 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL>
                                           const float *b_s, const float *kq_s, const int *par_s,
                                           unsigned tmem = 0) {
     if constexpr (TREE) {
+        constexpr int NV4 = RowState<DK, SL>::NV4;
+        const int j8 = (threadIdx.x & 31) & (kLanesPerRow - 1);
+        const size_t slot = (size_t)p.H_v * p.d_v * DK;
         const int *ord_s = par_s + (p.T + 1);  // depth-first order of the nodes
-        if constexpr (PARK) park_rows(rs, tmem);  // the loads issued at the item's start have landed by now
-        int prev = 0;
+        const int *plan_s = ord_s + p.T;
+        if constexpr (PARK) {
+            const int root_slot = plan_s[p.T];
+            if (root_slot >= 0) park_rows(rs, tmem, root_slot);  // the item's initial loads have landed by now
+        }
         for (int q = 0; q < p.T; ++q) {
-            const int node = ord_s[q];
-            recurrence_step<DK, TREE, SL, PARK>(p, rs, node - 1, prev, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s,
-                                                kq_s, par_s, tmem);
-            prev = node;
+            const int node = ord_s[q], pl = plan_s[q];
+            const int src = (int)(short)(pl & 0xffff), park = pl >> 16;
+            if (src >= 0) {
+                if constexpr (PARK) fetch_rows(rs, tmem, src);
+            } else if (src == -2) {
+                const int pp = par_s[node];
+                const float *from = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
+#pragma unroll
+                for (int s = 0; s < SL; ++s)
+#pragma unroll
+                    for (int m = 0; m < NV4; ++m)
+                        rs.S[s][m] = ld4(from + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
+            }
+            recurrence_step<DK, SL>(p, rs, node - 1, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s);
+            if constexpr (PARK) {
+                if (park >= 0) park_rows(rs, tmem, park);
+            }
         }
     } else {
-        for (int t = 0; t < p.T; ++t)
-            recurrence_step<DK, TREE, SL>(p, rs, t, t, s_in, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, par_s);
+        for (int t = 0; t < p.T; ++t) recurrence_step<DK, SL>(p, rs, t, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s);
     }
 }
 
@@ -410,15 +420,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     // work stealing: this CTA's own item first, then items of cancelled CTAs
     __shared__ __align__(16) unsigned long long steal_s[3];  // response (16 B), mbarrier
     __shared__ int next_s;
-    __shared__ unsigned park_s;  // tensor-memory columns of the parked initial rows (trees)
-    // Parking pays where an item's later root children would re-read its
-    // initial rows from DRAM: big launches. A small launch's checkpoints stay
-    // in L2, so the 4-rows-per-warp instantiation does not park.
-    constexpr bool kPark = TREE && SL == kSlots;
-    constexpr int kParkCols = 2 * RowState<DK, SL>::kWords <= 32    ? 32
-                              : 2 * RowState<DK, SL>::kWords <= 64  ? 64
-                              : 2 * RowState<DK, SL>::kWords <= 128 ? 128
-                                                                     : 256;
+    __shared__ unsigned park_s;  // tensor-memory columns of the parked branch points (trees)
+    // Tree branch points are parked in tensor memory: 2 states of 16 rows
+    // per warp (2 x 128 columns at d_k = 128, half of the SM's 512 for each
+    // of its 2 CTAs), 4 of 4 rows per warp (small launches). Two slots take
+    // all but ~0.4 % of the reloads of the random 23-node trees of the
+    // DDTree workload; the rest read the checkpoint.
+    constexpr bool kPark = TREE;
+    constexpr int kParkSlots = SL == kSlots ? 2 : 4;
+    constexpr int kParkWant = kParkSlots * 2 * RowState<DK, SL>::kWords;
+    constexpr int kParkCols = kParkWant <= 32 ? 32 : kParkWant <= 64 ? 64 : kParkWant <= 128 ? 128 : 256;
+    static_assert(kParkWant <= 256, "two CTAs per SM share its 512 tensor-memory columns");
     const unsigned resp = (unsigned)__cvta_generic_to_shared(steal_s);
     const unsigned bar = resp + 16;
     unsigned phase = 0;
@@ -428,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     if (it >= n_items) return;
     const Item I0 = decode_item(p, it, nrb);
     RowState<DK, SL> rs;
-    float ga = 0.f, gb = 0.f;
+    unsigned ga = 0u, gb = 0u;  // raw gates of the staged item
     int pr = 0;
     int tables_of = -1;  // request whose tree tables are in shared memory
     // Before the wait for the previous grid on the stream: with the caller's
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, T, kStageTaps);
         if constexpr (TREE) {
             pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I0.bidx * (T + 1) + tid]) : 0;
-            tree_tables(p, p.parent + (size_t)I0.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0);
+            tree_tables(p, p.parent + (size_t)I0.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0, kParkSlots);
             tables_of = I0.bidx;  // the barrier after the staging wait publishes them
         }
     }
@@ -484,13 +496,14 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
 
         cp_async_wait_all();
         if (tid < T) {
-            a_s[tid] = ga;
-            b_s[tid] = gb;
+            a_s[tid] = gate_value<BF16>(ga);
+            b_s[tid] = gate_value<BF16>(gb);
         }
         __syncthreads();  // staged inputs and gates visible to every thread
         if constexpr (TREE) {
             if (I.bidx != tables_of) {  // the tables depend on the request only
-                tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0);
+                tree_tables(p, p.parent + (size_t)I.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0,
+                            kParkSlots);
                 __syncthreads();
                 tables_of = I.bidx;
             }
@@ -629,9 +642,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
     norm_qk<DK>(p, q_s, k_s, kq_s, Te, threadIdx.x >> 5, blockDim.x >> 5);
     __syncthreads();
     if (has_rows) {
-        const float *s_in = p.ssm_out + head_off;
         for (int t = 0; t < Te; ++t)
-            recurrence_step<DK, false>(p, rs, t, t, s_in, nullptr, q_s, k_s, v_s, o_s, a_s, b_s, kq_s, nullptr);
+            recurrence_step<DK, kSlots>(p, rs, t, nullptr, q_s, k_s, v_s, o_s, a_s, b_s, kq_s);
         const int lane = tid & 31, j8 = lane & (kLanesPerRow - 1);
 #pragma unroll
         for (int s2 = 0; s2 < kSlots; ++s2)

@@ -76,6 +76,11 @@ __device__ __forceinline__ int item_channel(const VerifyArgs &p, const Item &I, 
 
 __host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
+// Ints of the tree-table region of shared memory for T processed nodes:
+// parents (T+1), the depth-first order (T), the reload plan (T+1) and six
+// scratch arrays of T+1.
+__host__ __device__ constexpr size_t tree_table_ints(int T) { return 9 * (size_t)T + 8; }
+
 // Shared-memory carve-up of the one-item-per-CTA kernel (byte offsets),
 // identical on host and device.
 struct Layout {
@@ -92,7 +97,7 @@ __host__ __device__ inline Layout make_layout(int T, int DK, int K) {
     L.a = off; off = al16(off + (size_t)T * 4);
     L.b = off; off = al16(off + (size_t)T * 4);
     L.kq = off; off = al16(off + (size_t)T * 4);
-    L.par = off; off = al16(off + (size_t)(2 * T + 1) * 4);  // parents, then the DFS order
+    L.par = off; off = al16(off + tree_table_ints(T) * 4);  // the tree tables
     L.src = off; off = al16(off + (size_t)T * K * 4);
     L.total = off;
     return L;
@@ -160,20 +165,47 @@ __device__ __forceinline__ int steal_result(unsigned resp, unsigned bar, unsigne
     return ok ? x : -1;
 }
 
-// Tree: validated parents -> par_s, and the conv-window table src_s:
-// position j of node i's window holds the input of the node at path depth
-// depth(i) - (K-1-j) when that is >= 1, else conv-state slot K-2 + that
-// depth (encoded -1 - slot). pg is the request's parent array in global
-// memory; `pr` is pg[tid] already loaded by this thread (when tid <= T).
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// tid / nthreads: this thread's rank in the calling group; the group syncs
-// on hardware barrier `bar` (0 with the whole block = __syncthreads).
+// Tree tables of one request, built by the calling group of threads
+// (tid / nthreads: this thread's rank; the group syncs on hardware barrier
+// `bar`, 0 with the whole block = __syncthreads), one thread per node:
+//  * par_s: the parents, validated (a parent outside [0, i) becomes i-1 and
+//    sets GDN_DEV_TREE). pg is the request's parent array in global memory;
+//    `pr` is pg[tid] already loaded by this thread (when tid <= T).
+//  * ord_s (= par_s + T+1): the depth-first preorder of nodes 1..T. A
+//    node's state is still in registers when its first child runs, and a
+//    parent's state is fetched again only on a branch switch. Children run
+//    in ascending order of subtree size (ties: lower index first), which
+//    keeps each fetch close in time to the write of the state it reads (48
+//    layers, 23 nodes: DRAM reads 245 -> 132 MB per launch with the root
+//    alone parked). A node's position is the sum, along its root path, of
+//    1 + the sizes of the siblings that run before each node on it.
+//  * plan_s (= ord_s + T): the reload plan of the recurrence. Entry q < T,
+//    for the q-th node n of the order, is (park << 16) | (src & 0xffff):
+//    src says where the state of parent(n) comes from when it is not the
+//    state just computed (-1: it is; k >= 0: tensor-memory slot k; -2: its
+//    checkpoint, or the initial state for the root), park >= 0 is the slot
+//    that keeps n's own state after its step, for its later children. Entry
+//    T is the slot of the initial (root) state, or -1. The slots form a
+//    stack of the branch points whose later children are still to run (a
+//    depth-first order returns to them innermost first); a branch point is
+//    parked when fewer than `cap` slots are taken at its step, i.e. when it
+//    has fewer than `cap` such branch points above it (an ancestor is one
+//    while the child on the way down is not its last), and then that count
+//    is its slot. cap = 0: every fetch reads memory.
+//  * src_s: the conv-window table: position j of node i's window holds the
+//    input of the node at path depth depth(i) - (K-1-j) when that is >= 1,
+//    else conv-state slot K-2 + that depth (encoded -1 - slot).
+// The caller syncs the group before anyone reads the tables.
 __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *pg, int pr, int *par_s,
-                                            int *src_s, int tid, int nthreads, int bar) {
+                                            int *src_s, int tid, int nthreads, int bar, int cap = 0) {
     const int T = p.T, K = p.K;
+    int *ord_s = par_s + (T + 1), *plan_s = ord_s + T;
+    int *size_s = plan_s + (T + 1), *nch_s = size_s + (T + 1), *off_s = nch_s + (T + 1);
+    int *pos_s = off_s + (T + 1), *last_s = pos_s + (T + 1), *slot_s = last_s + (T + 1);
     for (int i = tid; i <= T; i += nthreads) {
         int v = i == 0 ? -1 : (i == tid ? pr : pg[i]);
         if (i > 0 && (v < 0 || v >= i)) {
@@ -181,40 +213,56 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
             if (p.dev_status) atomicOr(p.dev_status, GDN_DEV_TREE);
         }
         par_s[i] = v;
+        size_s[i] = 1;
+        nch_s[i] = 0;
+        last_s[i] = 0;
     }
     bar_sync(bar, nthreads);
-    if (tid == 0) {
-        // Depth-first preorder of nodes 1..T: a node's state is still in
-        // registers when its first child runs, and a parent's state is
-        // reloaded (from its checkpoint) only on a branch switch. Children
-        // go in ascending order of subtree size (ties: lower index first),
-        // which keeps each reload close in time to the write of the state
-        // it reads, so that the checkpoint is still in L2 (48 layers, 23
-        // nodes: DRAM reads 245 -> 132 MB per launch).
-        int *ord_s = par_s + (T + 1);
-        int first[GDN_MAX_TOKENS + 1], next[GDN_MAX_TOKENS + 1], size[GDN_MAX_TOKENS + 1];
-        for (int i = 0; i <= T; ++i) {
-            first[i] = next[i] = -1;
-            size[i] = 1;
-        }
-        for (int i = T; i >= 1; --i) size[par_s[i]] += size[i];
-        for (int i = T; i >= 1; --i) {  // insert i among its siblings, ordered by (size, index)
-            int *link = &first[par_s[i]];
-            while (*link > 0 && (size[*link] < size[i] || (size[*link] == size[i] && *link < i))) link = &next[*link];
-            next[i] = *link;
-            *link = i;
-        }
-        int n = first[0], q = 0;
-        while (n > 0 && q < T) {
-            ord_s[q++] = n;
-            if (first[n] > 0) {
-                n = first[n];
-            } else {
-                while (n > 0 && next[n] < 0) n = par_s[n];
-                n = n > 0 ? next[n] : -1;
-            }
-        }
+    // subtree sizes and child counts: every node adds itself to its ancestors
+    for (int i = tid + 1; i <= T; i += nthreads) {
+        atomicAdd(&nch_s[par_s[i]], 1);
+        for (int a = par_s[i]; a >= 0; a = par_s[a]) atomicAdd(&size_s[a], 1);
     }
+    bar_sync(bar, nthreads);
+    // offset after the parent in the preorder; the sibling that runs last
+    for (int i = tid + 1; i <= T; i += nthreads) {
+        const int pp = par_s[i], si = size_s[i];
+        int off = 1;
+        bool last = true;
+        for (int j = 1; j <= T; ++j) {
+            if (j == i || par_s[j] != pp) continue;
+            const int sj = size_s[j];
+            if (sj < si || (sj == si && j < i)) off += sj;
+            else last = false;
+        }
+        off_s[i] = off;
+        if (last) last_s[pp] = i;
+    }
+    bar_sync(bar, nthreads);
+    // preorder positions; parking slots
+    for (int i = tid; i <= T; i += nthreads) {
+        if (i > 0) {
+            int pos = -1;
+            for (int a = i; a > 0; a = par_s[a]) pos += off_s[a];
+            pos_s[i] = pos;
+            ord_s[pos] = i;
+        }
+        int slot = -1;
+        if (cap > 0 && nch_s[i] >= 2) {
+            int open = 0;
+            for (int c = i, a = par_s[i]; a >= 0; c = a, a = par_s[a]) open += last_s[a] != c;
+            if (open < cap) slot = open;
+        }
+        slot_s[i] = slot;
+    }
+    bar_sync(bar, nthreads);
+    for (int i = tid + 1; i <= T; i += nthreads) {
+        const int pos = pos_s[i], pp = par_s[i];
+        const int prev = pos > 0 ? ord_s[pos - 1] : 0;
+        const int src = pp == prev ? -1 : (slot_s[pp] >= 0 ? slot_s[pp] : -2);
+        plan_s[pos] = (slot_s[i] << 16) | (src & 0xffff);
+    }
+    if (tid == 0) plan_s[T] = slot_s[0];
     for (int i = tid + 1; i <= T; i += nthreads) {
         int depth = 0;
         for (int n = i; n > 0; n = par_s[n]) ++depth;
@@ -367,16 +415,31 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
 
 // The small per-item values that are not contiguous: gates (thread t < T)
 // and, for trees, the parent array (thread i <= T); loaded into registers.
+// The gates stay raw (bf16 bits zero-extended, or f32 bits) until
+// gate_value() widens them, so that nothing waits for these loads before
+// the staging wait (a widening right after the load would expose its
+// latency).
 template <bool BF16, bool TREE>
-__device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item &I, float &ga, float &gb,
+__device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item &I, unsigned &ga, unsigned &gb,
                                                  int &pr, int tid) {
     const int T = p.T;
     if (tid < T) {
         const size_t gi = ((size_t)I.by * T + tid) * p.H_v + I.h;
-        ga = ld_in<BF16>(p.a, gi);
-        gb = ld_in<BF16>(p.b, gi);
+        if constexpr (BF16) {
+            ga = reinterpret_cast<const unsigned short *>(p.a)[gi];
+            gb = reinterpret_cast<const unsigned short *>(p.b)[gi];
+        } else {
+            ga = reinterpret_cast<const unsigned *>(p.a)[gi];
+            gb = reinterpret_cast<const unsigned *>(p.b)[gi];
+        }
     }
     if constexpr (TREE) pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I.bidx * (T + 1) + tid]) : 0;
+}
+
+// A raw gate from prefetch_scalars as f32 (bf16 -> f32 is exact).
+template <bool BF16>
+__device__ __forceinline__ float gate_value(unsigned raw) {
+    return BF16 ? __uint_as_float(raw << 16) : __uint_as_float(raw);
 }
 
 // Shared-memory carve-up of the work-stealing kernel: the item's buffers plus
@@ -396,7 +459,7 @@ __host__ __device__ inline PipeLayout make_pipe_layout(int T, int DK, int K, int
     L.a = off; off = al16(off + (size_t)T * 4);
     L.b = off; off = al16(off + (size_t)T * 4);
     L.kq = off; off = al16(off + (size_t)T * 4);
-    L.par = off; off = al16(off + (size_t)(2 * T + 1) * 4);  // parents, then the DFS order
+    L.par = off; off = al16(off + tree_table_ints(T) * 4);  // the tree tables
     L.src = off; off = al16(off + (size_t)T * K * 4);
     L.xst = off; off = al16(off + (size_t)T * XS * esize);
     L.wst = off; off = al16(off + XS * K * esize);

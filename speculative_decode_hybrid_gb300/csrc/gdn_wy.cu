@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
 
     // staged inputs (first cp.async group), then the state tile (second group)
     prefetch_item<DK, BF16>(p, I, xst, wst, cst, true, tid, nthreads, p.T);
-    float ga = 0.f, gb = 0.f;
+    unsigned ga = 0u, gb = 0u;  // raw gates of the staged item
     int pr = 0;
     prefetch_scalars<BF16, false>(p, I, ga, gb, pr, tid);
     for (int i = tid; i < I.R * U; i += nthreads) {
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
 
     asm volatile("cp.async.wait_group 1;" ::: "memory");  // the staged inputs have landed
     if (tid < T) {
-        a_s[tid] = ga;
-        b_s[tid] = gb;
+        a_s[tid] = gate_value<BF16>(ga);
+        b_s[tid] = gate_value<BF16>(gb);
     }
     __syncthreads();
     {
