@@ -364,6 +364,14 @@ def run_ours(args):
     step_bytes = (vbytes + st.accept_bytes() + st.restore_bytes(kn)) if not replay else st.replay_bytes(kl)
     step_gbs = step_bytes / (statistics.mean(gstep_ms) / 1e3) / 1e9
 
+    # ---- each kernel's cost inside the step graph (the eager per-kernel
+    #      events above include launch gaps that programmatic dependent
+    #      launch hides in the graph): graphs of the verify alone and of
+    #      verify -> accept, beside the whole step
+    parts = None
+    if graph_ok and rank == 0:
+        parts = graph_part_costs(st, args.commit, f_verify, flush, dev, stream, min(K, 50))
+
     # ---- end to end through the public API, host buffers, copies timed
     e2e = None
     if args.e2e_steps > 0:
@@ -400,7 +408,8 @@ def run_ours(args):
                      "restore_us_mean": statistics.mean(res_ms) * 1e3,
                      "restore_us_median": statistics.median(res_ms) * 1e3,
                      "eager_step_us_median": statistics.median(step_ms) * 1e3,
-                     "step_bytes": step_bytes, "step_gbs": step_gbs, "step_frac": step_gbs / hbm},
+                     "step_bytes": step_bytes, "step_gbs": step_gbs, "step_frac": step_gbs / hbm,
+                     "in_graph_us": parts},
         "e2e": e2e,
         "per_layer": per_layer,
         "mode": "cuda_graph" if graph_ok else "eager",
@@ -453,6 +462,47 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
             "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": 1e3 * statistics.mean(e2e_s),
             "ms_per_step_median": 1e3 * statistics.median(e2e_s),
             "mode": mode}
+
+
+def graph_part_costs(st, commit, f_verify, flush, dev, stream, n):
+    """Median µs of graph replays of the verify alone, of the verify with
+    either of the other two kernels and of the whole step, L2 flushed
+    between replays; the accept's and the commit's costs inside the step
+    are what each adds to the other two."""
+    import torch
+    main_graph = getattr(st, "_graph", None)
+    f_commit = {"checkpoint": st.restore, "replay": st.commit_replay, "wy": st.commit_wy}[commit]
+    ssm0, conv0 = st.ssm_state.clone(), st.conv_state.clone()
+    fns = {"verify": lambda stream=None: f_verify(stream),
+           "verify_accept": lambda stream=None: (f_verify(stream), st.accept(stream)),
+           "verify_commit": lambda stream=None: (f_verify(stream), f_commit(stream)),
+           "step": lambda stream=None: (f_verify(stream), st.accept(stream), f_commit(stream))}
+    out = {}
+    try:
+        for name, fn in fns.items():
+            st.step_fn = lambda c, fn=fn: fn
+            g = st.capture(name)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                g.replay()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+            out[name] = statistics.median([a.elapsed_time(b) for a, b in ev]) * 1e3
+            st.ssm_state.copy_(ssm0)
+            st.conv_state.copy_(conv0)
+    finally:
+        st.__dict__.pop("step_fn", None)  # the class's step_fn again
+        st._graph = main_graph
+    # the cost a kernel adds to the other two (its tail overlaps the next
+    # kernel's launch, so it is less than its own graph's end-to-end time)
+    out["accept"] = out["step"] - out["verify_commit"]
+    out["commit"] = out["step"] - out["verify_accept"]
+    return {k: round(v, 2) for k, v in out.items()}
 
 
 def run_per_layer(st, flush, dev, stream, K, units, ws):

@@ -267,8 +267,9 @@ size_t spec_accept_workspace_bytes(int32_t batch, int32_t n_nodes);
  * All calls share the one array: calls that may overlap on the GPU (other
  * streams, other host threads) race and must be serialised by the caller.
  * Returns GDN_ERR_WORKSPACE when spec_accept_workspace_bytes(batch, n_nodes)
- * exceeds GDN_STATIC_SCRATCH_BYTES (about 2,000 logit rows, e.g. batch 16 with
- * n_nodes up to 65 fits), and the other codes of spec_accept_greedy.
+ * exceeds GDN_STATIC_SCRATCH_BYTES (8 bytes per logit row plus 4 per
+ * request: about 130,000 rows, e.g. batch 2,000 with n_nodes 65 fits), and
+ * the other codes of spec_accept_greedy.
  */
 int spec_accept_greedy_static(int32_t batch, int32_t n_nodes, int32_t vocab,
                               const float *logits, const int32_t *tokens,

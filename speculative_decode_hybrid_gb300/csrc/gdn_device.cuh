@@ -35,6 +35,33 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// Fill L2 with the 128-byte lines of [base, base + bytes), the lines spread
+// over the group's threads. A prefetch only fills L2, the point of
+// coherence, and has no effect on what any load later returns.
+__device__ __forceinline__ void prefetch_l2_range(const void *base, size_t bytes, int tid, int nthreads) {
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(base) + bytes;
+    for (uintptr_t a = (reinterpret_cast<uintptr_t>(base) & ~uintptr_t(127)) + (uintptr_t)tid * 128u; a < a1;
+         a += (uintptr_t)nthreads * 128u)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+// The same with the L2 evict-last priority, for data that must survive a
+// stream of writes until it is read; the reader hands the lines back with
+// l2_normal_range() so that nothing stays ahead of other data.
+__device__ __forceinline__ void prefetch_l2_keep_range(const void *base, size_t bytes, int tid, int nthreads) {
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(base) + bytes;
+    for (uintptr_t a = (reinterpret_cast<uintptr_t>(base) & ~uintptr_t(127)) + (uintptr_t)tid * 128u; a < a1;
+         a += (uintptr_t)nthreads * 128u)
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(a));
+}
+
+__device__ __forceinline__ void l2_normal_range(const void *base, size_t bytes, int tid, int nthreads) {
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(base) + bytes;
+    for (uintptr_t a = (reinterpret_cast<uintptr_t>(base) & ~uintptr_t(127)) + (uintptr_t)tid * 128u; a < a1;
+         a += (uintptr_t)nthreads * 128u)
+        asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(a));
+}
+
 // Load element i of an input array stored as bf16 or f32, widened to f32
 // (bf16 -> f32 is exact).
 template <bool BF16>

@@ -609,16 +609,6 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
     }
 }
 
-// Fill L2 with the 128-byte lines of [base, base + bytes), the lines spread
-// over the group's threads. A prefetch only fills L2, the point of
-// coherence, and has no effect on what any load later returns.
-__device__ __forceinline__ void prefetch_l2_range(const void *base, size_t bytes, int tid, int nthreads) {
-    const uintptr_t a1 = reinterpret_cast<uintptr_t>(base) + bytes;
-    for (uintptr_t a = (reinterpret_cast<uintptr_t>(base) & ~uintptr_t(127)) + (uintptr_t)tid * 128u; a < a1;
-         a += (uintptr_t)nthreads * 128u)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-}
-
 // Warm L2 with item I's inputs: its state rows, x tile (all p.T nodes), conv
 // taps and conv state, gates and (tree) parents. Called before the kernel
 // waits for the previous grid on the stream: that grid may still be writing

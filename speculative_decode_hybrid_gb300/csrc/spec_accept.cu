@@ -9,13 +9,21 @@
 //    64-bit key  (order-preserving bits of the value << 32) | (~index),
 //    so a plain max picks the largest value and, among equal values, the
 //    lowest index; every NaN maps to the top value and the first NaN wins.
-//    -0.0 is folded into +0.0 so that equal values tie by index.
-//  * The CTA stores its key into the caller's workspace and bumps a
-//    per-request arrival counter. The last CTA of a request (threadfence +
-//    atomic counter, no spinning) reduces the keys of every row of that
-//    request, writes argmax_out, walks the chain or tree once and writes
-//    accept_len / accept_node, then puts the keys and the counter it used back
-//    to zero (so a later call of any shape finds a zero-filled workspace).
+//    -0.0 is folded into +0.0 so that equal values tie by index. Before it
+//    waits for the previous grid on the stream, the CTA prefetches its chunk
+//    into L2 with the evict-last priority (a prefetch only fills L2; the
+//    CTAs of this launch are resident well before that grid ends, which
+//    streams its writes until then) and sets it back to normal once read.
+//  * The CTA folds its key into its row's key in the caller's workspace
+//    (a 64-bit atomic max in L2) and bumps a per-request arrival counter.
+//    The last CTA of a request (threadfence + atomic counter, no spinning)
+//    reads the N row keys (one thread each), writes argmax_out, and decides
+//    the acceptance in parallel: a chain's accepted length is the number of
+//    leading matches (a warp ballot of the mismatches); a tree's nodes find
+//    their depth and whether their whole root path matches by walking to
+//    the root, one thread per node, and one thread picks the deepest
+//    matching node. It then puts the row keys and the counter back to zero
+//    (so a later call of any shape finds a zero-filled workspace).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -32,6 +40,7 @@ constexpr int kLoads = 4;                        // float4 loads in flight per t
 constexpr int kRoundLogits = kThreads * kLoads * 4;  // logits one CTA covers in one round
 constexpr int kMaxNodes = GDN_MAX_TOKENS + 1;
 static_assert(kMaxNodes <= kThreads, "one thread per node");
+constexpr int kBallotWarps = (kMaxNodes + 31) / 32;  // warps that cover the nodes of a chain
 constexpr size_t kCounterBytes(int32_t batch) { return (((size_t)batch * 4 + 255) / 256) * 256; }
 
 using gdndev::make_key;
@@ -51,24 +60,27 @@ __global__ void __launch_bounds__(kThreads)
 spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict__ logits,
                    const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
                    int32_t *argmax_out, int32_t *accept_len, int32_t *accept_node,
-                   unsigned *counters, unsigned long long *keys, int32_t *dev_status) {
+                   unsigned *counters, unsigned long long *rowkeys, int32_t *dev_status) {
     __shared__ unsigned long long red[kThreads / 32];
     __shared__ bool is_last;
-    __shared__ unsigned long long best_s[kMaxNodes];
-    __shared__ int am_s[kMaxNodes], par_s[kMaxNodes], dep_s[kMaxNodes], tok_s[kMaxNodes], pin_s[kMaxNodes];
-    __shared__ unsigned char ok_s[kMaxNodes];
+    __shared__ int am_s[kMaxNodes], par_s[kMaxNodes], dep_s[kMaxNodes], tok_s[kMaxNodes];
+    __shared__ unsigned char ok_s[kMaxNodes], bad_s[kMaxNodes];
+    __shared__ unsigned miss_s[kBallotWarps];
 
     const int split = blockIdx.x, n = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
+    const float *row = logits + ((size_t)b * N + n) * (size_t)V;
+    const int lo = split * chunk;
+    const int hi = min(V, lo + chunk);
+    // evict-last: the chunk must outlast the previous grid's writes (the
+    // verify streams its checkpoints at full bandwidth until it ends)
+    if (lo < hi) gdndev::prefetch_l2_keep_range(row + lo, (size_t)(hi - lo) * 4, tid, kThreads);
     gdndev::pdl_wait();
     gdndev::pdl_launch_dependents();  // the restore may be scheduled; it waits for this grid
     // the request's draft tokens / parents, loaded now so that the last CTA
     // does not wait for them after the ticket
     const int my_tok = tid < N ? tokens[(size_t)b * N + tid] : 0;
     const int my_par = tid < N ? (parent ? parent[(size_t)b * N + tid] : tid - 1) : 0;
-    const float *row = logits + ((size_t)b * N + n) * (size_t)V;
-    const int lo = split * chunk;
-    const int hi = min(V, lo + chunk);
 
     unsigned long long best = 0ull;  // below every real element
     if ((V & 3) == 0) {
@@ -96,6 +108,7 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     } else {
         for (int i = lo + tid; i < hi; i += kThreads) best = umax64(best, make_key(__ldcs(row + i), (unsigned)i));
     }
+    if (lo < hi) gdndev::l2_normal_range(row + lo, (size_t)(hi - lo) * 4, tid, kThreads);  // read: priority back
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, off));
     if ((tid & 31) == 0) red[tid >> 5] = best;
@@ -103,7 +116,7 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     if (tid == 0) {
         for (int w = 1; w < kThreads / 32; ++w) best = umax64(best, red[w]);
         if ((unsigned)(best >> 32) == 0xFFFFFFFFu && dev_status) atomicOr(dev_status, GDN_DEV_NAN_LOGIT);
-        keys[((size_t)b * N + n) * splits + split] = best;
+        atomicMax(&rowkeys[(size_t)b * N + n], best);  // the row's key: the max over its chunks
         __threadfence();
         const unsigned prev = atomicAdd(&counters[b], 1u);
         is_last = prev == (unsigned)(N * splits - 1);
@@ -112,69 +125,77 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     if (!is_last) return;
     __threadfence();
 
-    // ---- last CTA of request b: finish the argmax of every row and stage the
-    //      draft tokens / parents in shared memory (one load each, in parallel),
-    //      then walk
+    // ---- last CTA of request b: every chunk's max has landed in the row keys
     if (tid < N) {  // N <= kMaxNodes <= kThreads
-        best_s[tid] = 0ull;
-        tok_s[tid] = my_tok;
-        pin_s[tid] = my_par;
-    }
-    __syncthreads();
-    // every (row, chunk) key of the request, one independent load per thread
-    for (int i = tid; i < N * splits; i += kThreads) {
-        unsigned long long *kp = keys + (size_t)b * N * splits + i;
-        atomicMax(&best_s[i / splits], __ldcg(kp));
+        unsigned long long *kp = rowkeys + (size_t)b * N + tid;
+        const int am = (int)gdndev::key_index(__ldcg(kp));
         *kp = 0ull;  // leave the workspace zero-filled
+        am_s[tid] = am;
+        argmax_out[(size_t)b * N + tid] = am;
+        tok_s[tid] = my_tok;
+        // a tree node whose parent is outside [0, i) hangs under the root and
+        // never matches, nor does anything below it (flagged below)
+        const bool bad = tid > 0 && (my_par < 0 || my_par >= tid);
+        par_s[tid] = tid == 0 ? -1 : (bad ? 0 : my_par);
+        bad_s[tid] = bad ? 1 : 0;
     }
     __syncthreads();
-    for (int r = tid; r < N; r += kThreads) {
-        const int am = (int)(0xFFFFFFFFu - (unsigned)(best_s[r] & 0xFFFFFFFFull));
-        am_s[r] = am;
-        argmax_out[(size_t)b * N + r] = am;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const int *tok = tok_s;
-        int flags = 0;
-        int best_node = 0;
-        if (parent == nullptr) {
-            bool run = true;
-            for (int i = 1; i < N; ++i) {
-                const int t = tok[i];
-                if (t < 0 || t >= V) flags |= GDN_DEV_TOKEN_RANGE;
-                if (run && t == am_s[i - 1]) best_node = i;
-                else run = false;
+    if (parent == nullptr) {
+        // node i of a chain matches when its token is the argmax of row i - 1;
+        // k = the number of leading matches (a token outside [0, V) never matches)
+        if (tid < kBallotWarps * 32) {
+            const int i = tid;
+            const bool node = i >= 1 && i < N;
+            const int tk = node ? tok_s[i] : 0;
+            const bool range = node && (tk < 0 || tk >= V);
+            const unsigned miss = __ballot_sync(0xffffffffu, node && tk != am_s[node ? i - 1 : 0]);
+            const unsigned bad = __ballot_sync(0xffffffffu, range);
+            if ((tid & 31) == 0) {
+                miss_s[tid >> 5] = miss;
+                if (bad && dev_status) atomicOr(dev_status, GDN_DEV_TOKEN_RANGE);
             }
-            accept_len[b] = best_node;
-        } else {
-            const int *par = pin_s;
-            par_s[0] = -1;
-            dep_s[0] = 0;
-            ok_s[0] = 1;
-            for (int i = 1; i < N; ++i) {
-                const int t = tok[i];
-                if (t < 0 || t >= V) flags |= GDN_DEV_TOKEN_RANGE;
-                const int p = par[i];
-                if (p < 0 || p >= i) {  // bad geometry: the node never matches
-                    flags |= GDN_DEV_TREE;
-                    par_s[i] = 0;
-                    dep_s[i] = 1;
-                    ok_s[i] = 0;
-                    continue;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int k = N - 1;
+            for (int w = 0; w < kBallotWarps; ++w)
+                if (miss_s[w]) {
+                    k = 32 * w + __ffs((int)miss_s[w]) - 2;  // the first mismatching node, minus one
+                    break;
                 }
-                par_s[i] = p;
-                dep_s[i] = dep_s[p] + 1;
-                ok_s[i] = ok_s[p] && t == am_s[p];
+            accept_len[b] = k;
+            accept_node[b] = k;
+            counters[b] = 0u;  // leave the workspace zero-filled for the next call
+        }
+    } else {
+        // every node: its depth and whether its whole root path matches
+        // (tokens[j] == argmax of row parent(j) for every j on it)
+        if (tid < N) {
+            int flags = bad_s[tid] ? GDN_DEV_TREE : 0;
+            if (tid > 0 && (my_tok < 0 || my_tok >= V)) flags |= GDN_DEV_TOKEN_RANGE;
+            int dep = 0;
+            bool ok = true;
+            for (int j = tid; j > 0; j = par_s[j]) {
+                ++dep;
+                ok = ok && !bad_s[j] && tok_s[j] == am_s[par_s[j]];
+            }
+            dep_s[tid] = dep;
+            ok_s[tid] = ok ? 1 : 0;
+            if (flags && dev_status) atomicOr(dev_status, flags);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            // the deepest matching node; among equally deep ones the lower
+            // node index at the first divergence of their root paths
+            int best_node = 0;
+            for (int i = 1; i < N; ++i)
                 if (ok_s[i] && (dep_s[i] > dep_s[best_node] ||
                                 (dep_s[i] == dep_s[best_node] && path_less(par_s, i, best_node))))
                     best_node = i;
-            }
             accept_len[b] = dep_s[best_node];
+            accept_node[b] = best_node;
+            counters[b] = 0u;
         }
-        accept_node[b] = best_node;
-        if (flags && dev_status) atomicOr(dev_status, flags);
-        counters[b] = 0u;  // leave the workspace zero-filled for the next call
     }
 }
 
@@ -197,7 +218,7 @@ int choose_splits(int rows, int V) {
 
 extern "C" size_t spec_accept_workspace_bytes(int32_t batch, int32_t n_nodes) {
     if (batch < 1 || n_nodes < 1 || n_nodes > kMaxNodes || (int64_t)batch * n_nodes > (1 << 20)) return 0;
-    return kCounterBytes(batch) + (size_t)batch * n_nodes * kMaxSplits * sizeof(unsigned long long);
+    return kCounterBytes(batch) + (size_t)batch * n_nodes * sizeof(unsigned long long);  // counters, row keys
 }
 
 extern "C" int spec_accept_greedy(int32_t batch, int32_t n_nodes, int32_t vocab, const float *logits,
@@ -220,12 +241,12 @@ extern "C" int spec_accept_greedy(int32_t batch, int32_t n_nodes, int32_t vocab,
     int chunk = (vocab + splits - 1) / splits;
     chunk = (chunk + 3) & ~3;
     unsigned *counters = static_cast<unsigned *>(workspace);
-    unsigned long long *keys =
+    unsigned long long *rowkeys =
         reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + kCounterBytes(batch));
     dim3 grid(splits, n_nodes, batch);
     return gdndev::launch_pdl(spec_accept_kernel, grid, dim3(kThreads), 0, static_cast<cudaStream_t>(stream), n_nodes,
                               vocab, splits, chunk, logits, tokens, parent_dev, argmax_out, accept_len, accept_node,
-                              counters, keys, dev_status) == cudaSuccess
+                              counters, rowkeys, dev_status) == cudaSuccess
                ? GDN_OK
                : GDN_ERR_CUDA;
 }
@@ -289,19 +310,20 @@ extern "C" int spec_accept_greedy_static(int32_t batch, int32_t n_nodes, int32_t
     int rc = static_scratch(&scratch);
     if (rc != GDN_OK) return rc;
 
-    // The array keeps whatever the previous call left: zero the arrival
-    // counters (the only part that must start at zero) on the same stream.
+    // The array keeps whatever the previous call left (a completed call
+    // leaves the bytes it used at zero): zero the arrival counters and row
+    // keys of this call on the same stream all the same.
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, kCounterBytes(batch), st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, need, st) != cudaSuccess) return GDN_ERR_CUDA;
     const int splits = choose_splits(batch * n_nodes, vocab);
     int chunk = (vocab + splits - 1) / splits;
     chunk = (chunk + 3) & ~3;
     unsigned *counters = static_cast<unsigned *>(scratch);
-    unsigned long long *keys =
+    unsigned long long *rowkeys =
         reinterpret_cast<unsigned long long *>(static_cast<char *>(scratch) + kCounterBytes(batch));
     dim3 grid(splits, n_nodes, batch);
     spec_accept_kernel<<<grid, kThreads, 0, st>>>(n_nodes, vocab, splits, chunk, logits, tokens, parent_dev,
-                                                  argmax_out, accept_len, accept_node, counters, keys,
+                                                  argmax_out, accept_len, accept_node, counters, rowkeys,
                                                   dev_status);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

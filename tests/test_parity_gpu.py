@@ -395,6 +395,47 @@ def test_tree_device_parent_mismatch_is_flagged():
     assert int(st.dev_status.item()) & G.GDN_DEV_TREE
 
 
+def test_accept_bad_device_parent_excludes_its_subtree():
+    """A device parent outside [0, i) (the host copy valid) makes that node
+    and everything below it unmatched and flags GDN_DEV_TREE; the rest of the
+    acceptance is the oracle's on the same tree without that subtree. Every
+    drafted token matches its parent's argmax, so the deepest path would run
+    through the corrupted node."""
+    wl = W.draw(shape(n_nodes=23, tree=True, vocab=3000), seed=43)
+    par = wl.parent[0].copy()
+    am = np.array([oracle.argmax_f32(wl.logits[0, n]) for n in range(23)], dtype=np.int32)
+    tokens = wl.tokens.copy()
+    tokens[0, 1:] = am[par[1:]]
+    depth = oracle.tree_depths(par)[1]
+    deepest = int(np.argmax(depth))
+    node = deepest  # the child of the root on the way to the deepest node
+    while par[node] != 0:
+        node = int(par[node])
+    below = [i for i in range(1, 23) if node in _root_path(par, i)]
+    st = SpecStep(dataclasses.replace(wl, tokens=tokens))
+    bad = par.copy()
+    bad[node] = 50
+    st.parent.copy_(torch.from_numpy(bad[None, :]))
+    st.accept()
+    torch.cuda.synchronize()
+    want_tokens = tokens[0].copy()
+    for i in below:
+        want_tokens[i] = (am[par[i]] + 1) % wl.shape.vocab  # never the parent's argmax
+    o_am, o_kl, o_kn = oracle.accept_greedy(wl.logits[0], want_tokens, par)
+    np.testing.assert_array_equal(st.argmax[0].cpu().numpy(), o_am)
+    assert (int(st.accept_len[0]), int(st.accept_node[0])) == (o_kl, o_kn)
+    assert int(st.accept_node[0]) not in below
+    assert int(st.dev_status.item()) & G.GDN_DEV_TREE
+
+
+def _root_path(par, i):
+    path = []
+    while i > 0:
+        path.append(i)
+        i = int(par[i])
+    return path
+
+
 # ------------------------------------------------------------ both verify kernels
 
 def test_fallback_kernel_long_f32_span():

@@ -86,7 +86,9 @@ def test_static_rejects_sizes_beyond_its_scratch():
     lib = G.load()
     dev = torch.device("cuda")
     n = 65
-    batch = G.GDN_STATIC_SCRATCH_BYTES // (n * 64 * 8) + 1     # one request too many
+    batch = 1  # the smallest batch whose scratch no longer fits
+    while G.spec_accept_workspace_bytes(batch, n) <= G.GDN_STATIC_SCRATCH_BYTES:
+        batch += 1
     assert G.spec_accept_workspace_bytes(batch, n) > G.GDN_STATIC_SCRATCH_BYTES
     dummy = torch.zeros((16,), dtype=torch.float32, device=dev)
     with pytest.raises(G.GdnError) as e:
