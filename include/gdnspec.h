@@ -91,6 +91,8 @@ typedef void *gdn_stream_t;
 #define GDN_DEV_SCHED 0x10        /* verify: a CTA gave up waiting for an asynchronous hardware
                                      operation (the answer to a work-stealing request, or a
                                      tensor-core product); its outputs are incomplete */
+#define GDN_DEV_BOUNDS 0x20       /* debug builds of the library only (GDN_DEBUG_BOUNDS): a kernel
+                                     skipped a global access that fell outside its buffer */
 
 /* Limits of this library. */
 #define GDN_MAX_TOKENS 64         /* n_tok (= N - 1) per span */

@@ -5,7 +5,33 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "gdnspec.h"
+
 namespace gdndev {
+
+// A global buffer: its base and its size in bytes.
+struct Buf {
+    const void *base;
+    size_t bytes;
+};
+
+// Debug builds (compiled with GDN_DEBUG_BOUNDS) check every global access of
+// the kernels against the extent of its buffer first: an access of n bytes
+// at ptr that would not lie inside the buffer is skipped and GDN_DEV_BOUNDS
+// is OR-ed into the status word (when the caller passed one). There is no
+// trap. Release builds compile the checks away: GDN_IN is `true` there and
+// its arguments are never evaluated.
+#ifdef GDN_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_buf(const void *ptr, size_t n, Buf b, int32_t *status) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr), lo = reinterpret_cast<uintptr_t>(b.base);
+    const bool ok = b.base != nullptr && a >= lo && n <= b.bytes && a - lo <= b.bytes - n;
+    if (!ok && status) atomicOr(status, GDN_DEV_BOUNDS);
+    return ok;
+}
+#define GDN_IN(ptr, nbytes, buf, status) (::gdndev::in_buf((ptr), (nbytes), (buf), (status)))
+#else
+#define GDN_IN(ptr, nbytes, buf, status) true
+#endif
 
 // Programmatic dependent launch. pdl_wait(): wait until the kernels this
 // grid depends on (the previous work on the stream) have completed and their
@@ -76,6 +102,26 @@ __device__ __forceinline__ float ld_in(const void *p, size_t i) {
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// Checked accesses: GDN_IN first in debug builds (an access outside the
+// buffer is skipped; a load then returns zero), plain accesses in release
+// builds (the buffer arguments are pure arithmetic the compiler drops).
+__device__ __forceinline__ float4 ld4c(const float *p, Buf b, int32_t *st) {
+    return GDN_IN(p, 16, b, st) ? ld4(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ void st4c(float *p, float4 v, Buf b, int32_t *st) {
+    if (GDN_IN(p, 16, b, st)) st4(p, v);
+}
+__device__ __forceinline__ float ldfc(const float *p, Buf b, int32_t *st) { return GDN_IN(p, 4, b, st) ? *p : 0.f; }
+__device__ __forceinline__ void stfc(float *p, float v, Buf b, int32_t *st) {
+    if (GDN_IN(p, 4, b, st)) *p = v;
+}
+__device__ __forceinline__ int ldic(const int32_t *p, Buf b, int32_t *st) { return GDN_IN(p, 4, b, st) ? *p : 0; }
+template <bool BF16>
+__device__ __forceinline__ float ld_inc(const void *base, size_t i, Buf b, int32_t *st) {
+    return GDN_IN(static_cast<const char *>(base) + i * (BF16 ? 2 : 4), BF16 ? 2 : 4, b, st) ? ld_in<BF16>(base, i)
+                                                                                             : 0.f;
+}
 
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     acc = fmaf(a.x, b.x, acc);

@@ -26,17 +26,22 @@ constexpr int kCtasPerSm = 8;
 
 // Copy n4 16-byte vectors, this thread taking begin, begin + step, ...
 // (32-bit offsets: the host routes slots of 2^31 vectors or more elsewhere).
+// bs / bd: the source and destination buffers (bounds checks of debug builds).
 __device__ __forceinline__ void copy_range4(const float4 *__restrict__ src, float4 *__restrict__ dst,
-                                            unsigned n4, unsigned begin, unsigned step) {
+                                            unsigned n4, unsigned begin, unsigned step, gdndev::Buf bs,
+                                            gdndev::Buf bd, int32_t *st) {
     unsigned i = begin;
     for (; i + (kUnroll - 1) * step < n4; i += kUnroll * step) {
         float4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(src + i + u * step);
+        for (int u = 0; u < kUnroll; ++u)
+            v[u] = GDN_IN(src + i + u * step, 16, bs, st) ? __ldcs(src + i + u * step) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) dst[i + u * step] = v[u];
+        for (int u = 0; u < kUnroll; ++u)
+            if (GDN_IN(dst + i + u * step, 16, bd, st)) dst[i + u * step] = v[u];
     }
-    for (; i < n4; i += step) dst[i] = __ldcs(src + i);
+    for (; i < n4; i += step)
+        if (GDN_IN(src + i, 16, bs, st) && GDN_IN(dst + i, 16, bd, st)) dst[i] = __ldcs(src + i);
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -45,8 +50,13 @@ gdn_restore_kernel(int Y, int T, size_t ssm_slot, size_t conv_slot, const int32_
                    float *__restrict__ ssm_state, float *__restrict__ conv_state, int32_t *dev_status) {
     const int by = blockIdx.y;
     const int b = by / Y;
+    // buffer extents, for the bounds checks of debug builds (GDN_IN)
+    const size_t rows = gridDim.y;
+    const gdndev::Buf bsc{ssm_ckpt, rows * T * ssm_slot * 4}, bss{ssm_state, rows * ssm_slot * 4},
+        bcc{conv_ckpt, rows * T * conv_slot * 4}, bcs{conv_state, rows * conv_slot * 4},
+        bn{accept_node, rows / Y * 4};
     pdl_wait();  // accept_node and the checkpoints come from the kernels before
-    const int node = accept_node[b];
+    const int node = gdndev::ldic(accept_node + b, bn, dev_status);
     if (node == 0) return;
     if (node < 0 || node > T) {
         if (dev_status && blockIdx.x == 0 && by % Y == 0 && threadIdx.x == 0)
@@ -58,16 +68,17 @@ gdn_restore_kernel(int Y, int T, size_t ssm_slot, size_t conv_slot, const int32_
     {
         const float4 *src = reinterpret_cast<const float4 *>(ssm_ckpt + ((size_t)by * T + (node - 1)) * ssm_slot);
         float4 *dst = reinterpret_cast<float4 *>(ssm_state + (size_t)by * ssm_slot);
-        copy_range4(src, dst, (unsigned)(ssm_slot / 4), begin, step);
+        copy_range4(src, dst, (unsigned)(ssm_slot / 4), begin, step, bsc, bss, dev_status);
     }
     if (conv_slot > 0) {
         const float *src = conv_ckpt + ((size_t)by * T + (node - 1)) * conv_slot;
         float *dst = conv_state + (size_t)by * conv_slot;
         if ((conv_slot & 3) == 0) {
             copy_range4(reinterpret_cast<const float4 *>(src), reinterpret_cast<float4 *>(dst),
-                        (unsigned)(conv_slot / 4), begin, step);
+                        (unsigned)(conv_slot / 4), begin, step, bcc, bcs, dev_status);
         } else {
-            for (unsigned i = begin; i < conv_slot; i += step) dst[i] = src[i];
+            for (unsigned i = begin; i < conv_slot; i += step)
+                if (GDN_IN(src + i, 4, bcc, dev_status) && GDN_IN(dst + i, 4, bcs, dev_status)) dst[i] = src[i];
         }
     }
 }

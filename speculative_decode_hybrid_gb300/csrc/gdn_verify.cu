@@ -74,7 +74,7 @@ struct RowState {
 };
 
 template <int DK, int SL>
-__device__ __forceinline__ void load_rows(RowState<DK, SL> &rs, const float *src, bool has_rows) {
+__device__ __forceinline__ void load_rows(const VerifyArgs &p, RowState<DK, SL> &rs, const float *src, bool has_rows) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j8 = lane & (kLanesPerRow - 1), rsub = lane / kLanesPerRow;
 #pragma unroll
@@ -82,7 +82,8 @@ __device__ __forceinline__ void load_rows(RowState<DK, SL> &rs, const float *src
         rs.lrow[s] = warp * RowState<DK, SL>::kRows + s * kRowsPerSlot + rsub;
 #pragma unroll
         for (int m = 0; m < RowState<DK, SL>::NV4; ++m)
-            rs.S[s][m] = has_rows ? ld4(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m)
+            rs.S[s][m] = has_rows ? ld4c(src + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, buf_state<DK>(p),
+                                         p.dev_status)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
@@ -181,7 +182,7 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
             n.z = fmaf(c, kk[m].z, at * rs.S[s][m].z);
             n.w = fmaf(c, kk[m].w, at * rs.S[s][m].w);
             rs.S[s][m] = n;
-            if (p.ssm_ckpt) st4(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n);
+            if (p.ssm_ckpt) st4c(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n, buf_ckpt<DK>(p), p.dev_status);
         }
         if (j8 == 0) o_s[(size_t)t * kRowsPerCta + rs.lrow[s]] = fmaf(c, kqt, at * w[s]);
     }
@@ -218,11 +219,12 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL>
             } else if (src == -2) {
                 const int pp = par_s[node];
                 const float *from = pp == 0 ? s_in : ck0 + (size_t)(pp - 1) * slot;
+                const Buf fb = pp == 0 ? buf_state<DK>(p) : buf_ckpt<DK>(p);
 #pragma unroll
                 for (int s = 0; s < SL; ++s)
 #pragma unroll
                     for (int m = 0; m < NV4; ++m)
-                        rs.S[s][m] = ld4(from + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m);
+                        rs.S[s][m] = ld4c(from + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, fb, p.dev_status);
             }
             recurrence_step<DK, SL>(p, rs, node - 1, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s);
             if constexpr (PARK) {
@@ -241,8 +243,8 @@ __device__ __forceinline__ void write_out(const VerifyArgs &p, const Item &I, co
     const int r4 = I.R / 4;
     for (int i = tid; i < p.T * r4; i += nthreads) {
         const int t = i / r4, r = (i - t * r4) * 4;
-        st4(p.out + (((size_t)I.by * p.T + t) * p.H_v + I.h) * p.d_v + I.row0 + r,
-            ld4(o_s + (size_t)t * kRowsPerCta + r));
+        st4c(p.out + (((size_t)I.by * p.T + t) * p.H_v + I.h) * p.d_v + I.row0 + r,
+             ld4(o_s + (size_t)t * kRowsPerCta + r), buf_out(p), p.dev_status);
     }
 }
 
@@ -271,17 +273,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
     const bool has_rows = warp * kRowsPerWarp < I.R;
     const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
     RowState<DK> rs;
-    load_rows<DK>(rs, p.ssm_in + head_off, has_rows);
+    load_rows<DK>(p, rs, p.ssm_in + head_off, has_rows);
 
     if constexpr (TREE) {
         const int32_t *pg = p.parent + (size_t)I.bidx * (T + 1);
-        const int pr = tid <= T ? (tid == 0 ? -1 : pg[tid]) : 0;
+        const int pr = tid <= T ? (tid == 0 ? -1 : ldic(pg + tid, buf_parent(p), p.dev_status)) : 0;
         tree_tables(p, pg, pr, par_s, src_s, tid, nthreads, 0);
     }
     for (int t = tid; t < T; t += nthreads) {
         const size_t gi = ((size_t)I.by * T + t) * p.H_v + I.h;
-        a_s[t] = ld_in<BF16>(p.a, gi);
-        b_s[t] = ld_in<BF16>(p.b, gi);
+        a_s[t] = ld_inc<BF16>(p.a, gi, buf_a<BF16 ? 2 : 4>(p), p.dev_status);
+        b_s[t] = ld_inc<BF16>(p.b, gi, buf_b<BF16 ? 2 : 4>(p), p.dev_status);
     }
     if constexpr (TREE) __syncthreads();  // src_s ready
 
@@ -300,8 +302,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
             float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
 #pragma unroll
             for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
-                wr[j] = j < K ? ld_in<BF16>(p.w, ((size_t)I.y * p.C + c) * K + j) : 0.f;
-                st[j] = j < K - 1 ? p.conv_in[((size_t)I.by * p.C + c) * (K - 1) + j] : 0.f;
+                wr[j] = j < K ? ld_inc<BF16>(p.w, ((size_t)I.y * p.C + c) * K + j, buf_w<BF16 ? 2 : 4>(p), p.dev_status)
+                              : 0.f;
+                st[j] = j < K - 1 ? ldfc(p.conv_in + ((size_t)I.by * p.C + c) * (K - 1) + j, buf_conv(p), p.dev_status)
+                                  : 0.f;
             }
             float *cck = p.conv_ckpt + (size_t)I.by * T * cc_tok + (size_t)c * (K - 1);
             if constexpr (!TREE) {
@@ -310,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
                     float xr[CH];
 #pragma unroll
                     for (int u = 0; u < CH; ++u)
-                        xr[u] = t0 + u < T ? ld_in<BF16>(xin, x_base + (size_t)(t0 + u) * p.C + c) : 0.f;
+                        xr[u] = t0 + u < T ? ld_inc<BF16>(xin, x_base + (size_t)(t0 + u) * p.C + c,
+                                                          buf_x<BF16 ? 2 : 4>(p), p.dev_status)
+                                           : 0.f;
 #pragma unroll
                     for (int u = 0; u < CH; ++u) {
                         const int t = t0 + u;
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
                             if (own) {
 #pragma unroll
                                 for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
-                                    if (j < K - 1) cck[(size_t)t * cc_tok + j] = st[j];
+                                    if (j < K - 1) stfc(cck + (size_t)t * cc_tok + j, st[j], buf_cckpt(p), p.dev_status);
                             }
                         }
                     }
@@ -344,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
                             if (t0 + u < T && j < K) {
                                 const int s = src_s[(t0 + u) * K + j];
                                 if (s >= 1) {
-                                    v = ld_in<BF16>(xin, x_base + (size_t)(s - 1) * p.C + c);
+                                    v = ld_inc<BF16>(xin, x_base + (size_t)(s - 1) * p.C + c, buf_x<BF16 ? 2 : 4>(p),
+                                                     p.dev_status);
                                 } else {
                                     const int slot = -1 - s;
 #pragma unroll
@@ -363,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
                             if (own) {
 #pragma unroll
                                 for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
-                                    if (j < K - 1) cck[(size_t)t * cc_tok + j] = wv[u][j + 1];
+                                    if (j < K - 1)
+                                        stfc(cck + (size_t)t * cc_tok + j, wv[u][j + 1], buf_cckpt(p), p.dev_status);
                             }
                         }
                     }
@@ -452,11 +460,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     const bool early = !RP && p.early;
     prefetch_l2_item<DK, BF16, TREE>(p, I0, tid, nthreads, !early);
     if (early) {
-        load_rows(rs, p.ssm_in + ((size_t)I0.by * p.H_v + I0.h) * (size_t)p.d_v * DK + (size_t)I0.row0 * DK,
+        load_rows(p, rs, p.ssm_in + ((size_t)I0.by * p.H_v + I0.h) * (size_t)p.d_v * DK + (size_t)I0.row0 * DK,
                   warp * RowState<DK, SL>::kRows < I0.R);
         prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, T, kStageTaps);
         if constexpr (TREE) {
-            pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I0.bidx * (T + 1) + tid]) : 0;
+            pr = tid <= T ? (tid == 0 ? -1 : ldic(p.parent + (size_t)I0.bidx * (T + 1) + tid, buf_parent(p), p.dev_status))
+                          : 0;
             tree_tables(p, p.parent + (size_t)I0.bidx * (T + 1), pr, par_s, src_s, tid, nthreads, 0, kParkSlots);
             tables_of = I0.bidx;  // the barrier after the staging wait publishes them
         }
@@ -473,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     // the tokens an item runs: all of them, or (replay) the accepted ones
     auto tokens_of = [&](const Item &J) -> int {
         if constexpr (!RP) return T;
-        const int k = p.accept_len[J.bidx];
+        const int k = ldic(p.accept_len + J.bidx, buf_accept(p), p.dev_status);
         return k >= 0 && k <= T ? k : 0;  // out of range: flagged below, nothing changes
     };
     VerifyArgs pn = p;  // p with T = the staged item's tokens
@@ -485,13 +494,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         const Item I = decode_item(p, it, nrb);
         const VerifyArgs pi = pn;  // this item's token count (pn moves on to the next item)
         if constexpr (RP) {
-            const int k = p.accept_len[I.bidx];
+            const int k = ldic(p.accept_len + I.bidx, buf_accept(p), p.dev_status);
             if ((k < 0 || k > T) && p.dev_status && tid == 0 && I.y == 0 && I.h == 0 && I.rb == 0)
                 atomicOr(p.dev_status, GDN_DEV_NODE_RANGE);
         }
         const bool has_rows = warp * RowState<DK, SL>::kRows < I.R && pi.T > 0;
         const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-        if (!rows_ready) load_rows(rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
+        if (!rows_ready) load_rows(p, rs, p.ssm_in + head_off, has_rows);  // overlaps the prologue
         rows_ready = false;
 
         cp_async_wait_all();
@@ -550,7 +559,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
                 for (int s2 = 0; s2 < SL; ++s2)
 #pragma unroll
                     for (int m = 0; m < RowState<DK, SL>::NV4; ++m)
-                        st4(p.ssm_out + head_off + (size_t)rs.lrow[s2] * DK + 4 * j8 + kColStride * m, rs.S[s2][m]);
+                        st4c(p.ssm_out + head_off + (size_t)rs.lrow[s2] * DK + 4 * j8 + kColStride * m, rs.S[s2][m],
+                             buf_state<DK>(p), p.dev_status);
             }
         }
         __syncthreads();
@@ -586,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
     const int nrb = row_blocks(p);
     const Item I = decode_item(p, (blockIdx.z * p.H_v + blockIdx.y) * nrb + blockIdx.x, nrb);
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
-    const int Te = accept_len[I.bidx];
+    const int Te = ldic(accept_len + I.bidx, buf_accept(p), p.dev_status);
     if (Te <= 0 || Te > T) {
         if (Te != 0 && p.dev_status && tid == 0 && I.y == 0 && I.h == 0 && I.rb == 0)
             atomicOr(p.dev_status, GDN_DEV_NODE_RANGE);
@@ -595,11 +605,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
     const bool has_rows = warp * kRowsPerWarp < I.R;
     const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
     RowState<DK> rs;
-    load_rows<DK>(rs, p.ssm_out + head_off, has_rows);
+    load_rows<DK>(p, rs, p.ssm_out + head_off, has_rows);
     for (int t = tid; t < Te; t += nthreads) {
         const size_t gi = ((size_t)I.by * T + t) * p.H_v + I.h;
-        a_s[t] = ld_in<BF16>(p.a, gi);
-        b_s[t] = ld_in<BF16>(p.b, gi);
+        a_s[t] = ld_inc<BF16>(p.a, gi, buf_a<BF16 ? 2 : 4>(p), p.dev_status);
+        b_s[t] = ld_inc<BF16>(p.b, gi, buf_b<BF16 ? 2 : 4>(p), p.dev_status);
     }
     {
         const int nch = 2 * DK + I.R;
@@ -611,15 +621,19 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
             float wr[GDN_MAX_CONV_K], st[GDN_MAX_CONV_K];
 #pragma unroll
             for (int j = 0; j < GDN_MAX_CONV_K; ++j) {
-                wr[j] = j < K ? ld_in<BF16>(p.w, ((size_t)I.y * p.C + c) * K + j) : 0.f;
-                st[j] = j < K - 1 ? p.conv_in[((size_t)I.by * p.C + c) * (K - 1) + j] : 0.f;
+                wr[j] = j < K ? ld_inc<BF16>(p.w, ((size_t)I.y * p.C + c) * K + j, buf_w<BF16 ? 2 : 4>(p), p.dev_status)
+                              : 0.f;
+                st[j] = j < K - 1 ? ldfc(p.conv_in + ((size_t)I.by * p.C + c) * (K - 1) + j, buf_conv(p), p.dev_status)
+                                  : 0.f;
             }
             constexpr int CH = 8;
             for (int t0 = 0; t0 < Te; t0 += CH) {
                 float xr[CH];
 #pragma unroll
                 for (int u = 0; u < CH; ++u)
-                    xr[u] = t0 + u < Te ? ld_in<BF16>(p.x, x_base + (size_t)(t0 + u) * p.C + c) : 0.f;
+                    xr[u] = t0 + u < Te ? ld_inc<BF16>(p.x, x_base + (size_t)(t0 + u) * p.C + c, buf_x<BF16 ? 2 : 4>(p),
+                                                       p.dev_status)
+                                        : 0.f;
 #pragma unroll
                 for (int u = 0; u < CH; ++u) {
                     const int t = t0 + u;
@@ -649,7 +663,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_replay_kernel(const VerifyArg
         for (int s2 = 0; s2 < kSlots; ++s2)
 #pragma unroll
             for (int m = 0; m < RowState<DK>::NV4; ++m)
-                st4(p.ssm_out + head_off + (size_t)rs.lrow[s2] * DK + 4 * j8 + kColStride * m, rs.S[s2][m]);
+                st4c(p.ssm_out + head_off + (size_t)rs.lrow[s2] * DK + 4 * j8 + kColStride * m, rs.S[s2][m],
+                     buf_state<DK>(p), p.dev_status);
     }
 }
 

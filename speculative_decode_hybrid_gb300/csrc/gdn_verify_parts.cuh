@@ -29,6 +29,7 @@ constexpr size_t kStaticSmem = 64;  // the work-stealing kernel's static shared 
 static_assert(kRowsPerWarp <= 16 && 16 % kRowsPerWarp == 0, "d_v is validated as a multiple of 16");
 
 struct VerifyArgs {
+    int B, Tb;              // requests; tokens of the call's buffers (T itself may be fewer: a replay's k)
     int Y, H_k, H_v, d_v, C, K, T;
     float q_scale;
     const void *x, *a, *b, *w;
@@ -73,6 +74,30 @@ __device__ __forceinline__ int item_channel(const VerifyArgs &p, const Item &I, 
     if (lc < 2 * DK) return p.H_k * DK + I.g * DK + (lc - DK);
     return 2 * p.H_k * DK + I.h * p.d_v + I.row0 + (lc - 2 * DK);
 }
+
+// Extents of the argument buffers, for the bounds checks of debug builds
+// (GDN_IN; never evaluated in release builds). ES: bytes per input element;
+// DK: the key head size.
+__device__ __forceinline__ size_t n_by(const VerifyArgs &p) { return (size_t)p.B * p.Y; }
+template <int ES>
+__device__ __forceinline__ Buf buf_x(const VerifyArgs &p) { return {p.x, n_by(p) * p.Tb * p.C * ES}; }
+template <int ES>
+__device__ __forceinline__ Buf buf_a(const VerifyArgs &p) { return {p.a, n_by(p) * p.Tb * p.H_v * ES}; }
+template <int ES>
+__device__ __forceinline__ Buf buf_b(const VerifyArgs &p) { return {p.b, n_by(p) * p.Tb * p.H_v * ES}; }
+template <int ES>
+__device__ __forceinline__ Buf buf_w(const VerifyArgs &p) { return {p.w, (size_t)p.Y * p.C * p.K * ES}; }
+template <int DK>
+__device__ __forceinline__ Buf buf_state(const VerifyArgs &p) { return {p.ssm_in, n_by(p) * p.H_v * p.d_v * DK * 4}; }
+__device__ __forceinline__ Buf buf_conv(const VerifyArgs &p) { return {p.conv_in, n_by(p) * p.C * (p.K - 1) * 4}; }
+template <int DK>
+__device__ __forceinline__ Buf buf_ckpt(const VerifyArgs &p) {
+    return {p.ssm_ckpt, n_by(p) * p.Tb * p.H_v * p.d_v * DK * 4};
+}
+__device__ __forceinline__ Buf buf_cckpt(const VerifyArgs &p) { return {p.conv_ckpt, n_by(p) * p.Tb * p.C * (p.K - 1) * 4}; }
+__device__ __forceinline__ Buf buf_out(const VerifyArgs &p) { return {p.out, n_by(p) * p.Tb * p.H_v * p.d_v * 4}; }
+__device__ __forceinline__ Buf buf_parent(const VerifyArgs &p) { return {p.parent, (size_t)p.B * (p.Tb + 1) * 4}; }
+__device__ __forceinline__ Buf buf_accept(const VerifyArgs &p) { return {p.accept_len, (size_t)p.B * 4}; }
 
 __host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -207,7 +232,7 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
     int *size_s = plan_s + (T + 1), *nch_s = size_s + (T + 1), *off_s = nch_s + (T + 1);
     int *pos_s = off_s + (T + 1), *last_s = pos_s + (T + 1), *slot_s = last_s + (T + 1);
     for (int i = tid; i <= T; i += nthreads) {
-        int v = i == 0 ? -1 : (i == tid ? pr : pg[i]);
+        int v = i == 0 ? -1 : (i == tid ? pr : ldic(pg + i, buf_parent(p), p.dev_status));
         if (i > 0 && (v < 0 || v >= i)) {
             v = i - 1;
             if (p.dev_status) atomicOr(p.dev_status, GDN_DEV_TREE);
@@ -383,8 +408,8 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
             if (r < cq) { c0 = c_q; dch = 0; off = r; }
             else if (r < 2 * cq) { c0 = c_k; dch = DK; off = r - cq; }
             else { c0 = c_v; dch = 2 * DK; off = r - 2 * cq; }
-            cp_async16(xst + ((size_t)t * XS + dch) * ES + (size_t)off * 16,
-                       xg + (((size_t)I.by * T + t) * p.C + c0) * ES + (size_t)off * 16);
+            const unsigned char *src = xg + (((size_t)I.by * T + t) * p.C + c0) * ES + (size_t)off * 16;
+            if (GDN_IN(src, 16, buf_x<ES>(p), p.dev_status)) cp_async16(xst + ((size_t)t * XS + dch) * ES + (size_t)off * 16, src);
         }
     }
     // conv taps [c][K] and conv state [c][K-1] of the three ranges
@@ -396,8 +421,8 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
             if (i < wq) { c0 = c_q; dch = 0; off = i; }
             else if (i < 2 * wq) { c0 = c_k; dch = DK; off = i - wq; }
             else { c0 = c_v; dch = 2 * DK; off = i - 2 * wq; }
-            cp_async16(wst + (size_t)dch * K * ES + (size_t)off * 16,
-                       wg + ((size_t)I.y * p.C + c0) * K * ES + (size_t)off * 16);
+            const unsigned char *src = wg + ((size_t)I.y * p.C + c0) * K * ES + (size_t)off * 16;
+            if (GDN_IN(src, 16, buf_w<ES>(p), p.dev_status)) cp_async16(wst + (size_t)dch * K * ES + (size_t)off * 16, src);
         }
         const int sq = DK * (K - 1) * 4 / 16, sv = I.R * (K - 1) * 4 / 16, sn = 2 * sq + sv;
         for (int i = (with_qk ? 0 : 2 * sq) + tid; i < sn; i += nthreads) {
@@ -406,8 +431,8 @@ __device__ __forceinline__ void prefetch_item(const VerifyArgs &p, const Item &I
             if (i < sq) { c0 = c_q; dch = 0; off = i; }
             else if (i < 2 * sq) { c0 = c_k; dch = DK; off = i - sq; }
             else { c0 = c_v; dch = 2 * DK; off = i - 2 * sq; }
-            cp_async16(cst + (size_t)dch * (K - 1) * 4 + (size_t)off * 16,
-                       cg + ((size_t)I.by * p.C + c0) * (K - 1) * 4 + (size_t)off * 16);
+            const unsigned char *src = cg + ((size_t)I.by * p.C + c0) * (K - 1) * 4 + (size_t)off * 16;
+            if (GDN_IN(src, 16, buf_conv(p), p.dev_status)) cp_async16(cst + (size_t)dch * (K - 1) * 4 + (size_t)off * 16, src);
         }
     }
     cp_async_commit();
@@ -425,15 +450,20 @@ __device__ __forceinline__ void prefetch_scalars(const VerifyArgs &p, const Item
     const int T = p.T;
     if (tid < T) {
         const size_t gi = ((size_t)I.by * T + tid) * p.H_v + I.h;
+        constexpr int ES = BF16 ? 2 : 4;
+        const bool ina = GDN_IN(static_cast<const char *>(p.a) + gi * ES, ES, buf_a<ES>(p), p.dev_status);
+        const bool inb = GDN_IN(static_cast<const char *>(p.b) + gi * ES, ES, buf_b<ES>(p), p.dev_status);
         if constexpr (BF16) {
-            ga = reinterpret_cast<const unsigned short *>(p.a)[gi];
-            gb = reinterpret_cast<const unsigned short *>(p.b)[gi];
+            ga = ina ? reinterpret_cast<const unsigned short *>(p.a)[gi] : 0u;
+            gb = inb ? reinterpret_cast<const unsigned short *>(p.b)[gi] : 0u;
         } else {
-            ga = reinterpret_cast<const unsigned *>(p.a)[gi];
-            gb = reinterpret_cast<const unsigned *>(p.b)[gi];
+            ga = ina ? reinterpret_cast<const unsigned *>(p.a)[gi] : 0u;
+            gb = inb ? reinterpret_cast<const unsigned *>(p.b)[gi] : 0u;
         }
     }
-    if constexpr (TREE) pr = tid <= T ? (tid == 0 ? -1 : p.parent[(size_t)I.bidx * (T + 1) + tid]) : 0;
+    if constexpr (TREE)
+        pr = tid <= T ? (tid == 0 ? -1 : ldic(p.parent + (size_t)I.bidx * (T + 1) + tid, buf_parent(p), p.dev_status))
+                      : 0;
 }
 
 // A raw gate from prefetch_scalars as f32 (bf16 -> f32 is exact).
@@ -575,7 +605,7 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
                             const float xv = src[j] >= 0 ? ld_in<BF16>(xst, (size_t)src[j] * XS + c)
                                                          : cstf[(size_t)c * (K - 1) + (-1 - src[j])];
                             a = fmaf(w[j], xv, a);
-                            if (cc && j >= 1) cc[j - 1] = xv;
+                            if (cc && j >= 1) stfc(cc + (j - 1), xv, buf_cckpt(p), p.dev_status);
                         }
                     }
                     acc[hf][e] = silu(a);
@@ -601,7 +631,7 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
                     const float xv = src[j] >= 0 ? ld_in<BF16>(xst, (size_t)src[j] * XS + c)
                                                  : cstf[(size_t)c * (K - 1) + (-1 - src[j])];
                     acc = fmaf(w[j], xv, acc);
-                    if (cv && j >= 1) cv[j - 1] = xv;
+                    if (cv && j >= 1) stfc(cv + (j - 1), xv, buf_cckpt(p), p.dev_status);
                 }
             }
             v_s[(size_t)t * kRowsPerCta + lc] = silu(acc);
@@ -622,14 +652,17 @@ __device__ __forceinline__ void prefetch_l2_item(const VerifyArgs &p, const Item
     constexpr int ES = BF16 ? 2 : 4;
     const int T = p.T, K = p.K;
     const size_t head_off = ((size_t)I.by * p.H_v + I.h) * (size_t)p.d_v * DK + (size_t)I.row0 * DK;
-    if (with_state) prefetch_l2_range(p.ssm_in + head_off, (size_t)I.R * DK * 4, tid, nthreads);
+    if (with_state && GDN_IN(p.ssm_in + head_off, (size_t)I.R * DK * 4, buf_state<DK>(p), p.dev_status))
+        prefetch_l2_range(p.ssm_in + head_off, (size_t)I.R * DK * 4, tid, nthreads);
     const size_t c_q = (size_t)I.g * DK, c_k = (size_t)p.H_k * DK + c_q;
     const size_t c_v = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;
     const unsigned char *xg = static_cast<const unsigned char *>(p.x);
     for (int i = tid; i < 3 * T; i += nthreads) {  // (node, channel range) pairs
         const int t = i / 3, r = i - 3 * t;
         const size_t c0 = r == 0 ? c_q : r == 1 ? c_k : c_v;
-        prefetch_l2_range(xg + (((size_t)I.by * T + t) * p.C + c0) * ES, (r < 2 ? DK : I.R) * (size_t)ES, 0, 1);
+        const unsigned char *xa = xg + (((size_t)I.by * T + t) * p.C + c0) * ES;
+        const size_t xn = (r < 2 ? DK : I.R) * (size_t)ES;
+        if (GDN_IN(xa, xn, buf_x<ES>(p), p.dev_status)) prefetch_l2_range(xa, xn, 0, 1);
     }
     const unsigned char *wg = static_cast<const unsigned char *>(p.w);
     const int sub = tid & 31, lanes = 32;  // small ranges: one warp each
@@ -638,18 +671,24 @@ __device__ __forceinline__ void prefetch_l2_item(const VerifyArgs &p, const Item
     for (int r = w; with_state && r < 6; r += nw) {
         const size_t c0 = (r % 3) == 0 ? c_q : (r % 3) == 1 ? c_k : c_v;
         const size_t n = (r % 3) == 2 ? (size_t)I.R : (size_t)DK;
-        if (r < 3)
-            prefetch_l2_range(wg + ((size_t)I.y * p.C + c0) * K * ES, n * K * ES, sub, lanes);
-        else if (p.conv_in && K > 1)
-            prefetch_l2_range(p.conv_in + ((size_t)I.by * p.C + c0) * (K - 1), n * (K - 1) * 4, sub, lanes);
+        if (r < 3) {
+            if (GDN_IN(wg + ((size_t)I.y * p.C + c0) * K * ES, n * K * ES, buf_w<ES>(p), p.dev_status))
+                prefetch_l2_range(wg + ((size_t)I.y * p.C + c0) * K * ES, n * K * ES, sub, lanes);
+        } else if (p.conv_in && K > 1) {
+            if (GDN_IN(p.conv_in + ((size_t)I.by * p.C + c0) * (K - 1), n * (K - 1) * 4, buf_conv(p), p.dev_status))
+                prefetch_l2_range(p.conv_in + ((size_t)I.by * p.C + c0) * (K - 1), n * (K - 1) * 4, sub, lanes);
+        }
     }
     if (tid < T) {
         const size_t gi = ((size_t)I.by * T + tid) * p.H_v + I.h;
-        prefetch_l2_range(static_cast<const unsigned char *>(p.a) + gi * ES, ES, 0, 1);
-        prefetch_l2_range(static_cast<const unsigned char *>(p.b) + gi * ES, ES, 0, 1);
+        if (GDN_IN(static_cast<const unsigned char *>(p.a) + gi * ES, ES, buf_a<ES>(p), p.dev_status))
+            prefetch_l2_range(static_cast<const unsigned char *>(p.a) + gi * ES, ES, 0, 1);
+        if (GDN_IN(static_cast<const unsigned char *>(p.b) + gi * ES, ES, buf_b<ES>(p), p.dev_status))
+            prefetch_l2_range(static_cast<const unsigned char *>(p.b) + gi * ES, ES, 0, 1);
     }
     if constexpr (TREE) {
-        if (tid == 0) prefetch_l2_range(p.parent + (size_t)I.bidx * (T + 1), (size_t)(T + 1) * 4, 0, 1);
+        if (tid == 0 && GDN_IN(p.parent + (size_t)I.bidx * (T + 1), (size_t)(T + 1) * 4, buf_parent(p), p.dev_status))
+            prefetch_l2_range(p.parent + (size_t)I.bidx * (T + 1), (size_t)(T + 1) * 4, 0, 1);
     }
 }
 
@@ -683,6 +722,8 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
                      const void *w, const float *ssm_in, const float *conv_in, float *ssm_ckpt,
                      float *conv_ckpt, float *out, const int32_t *parent, int32_t *dev_status) {
     VerifyArgs v;
+    v.B = d->batch;
+    v.Tb = T;
     v.Y = d->layers;
     v.H_k = d->h_k;
     v.H_v = d->h_v;
@@ -719,7 +760,7 @@ __global__ void __launch_bounds__(256) gdn_conv_state_kernel(const VerifyArgs p,
     const int by = blockIdx.y, bidx = by / p.Y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     const int K = p.K, T = p.T;
-    const int k = accept_len[bidx];
+    const int k = ldic(accept_len + bidx, buf_accept(p), p.dev_status);
     if (c >= p.C || k <= 0 || k > T) return;
     float *cs = conv_state + ((size_t)by * p.C + c) * (K - 1);
     float nw[GDN_MAX_CONV_K];
@@ -728,12 +769,13 @@ __global__ void __launch_bounds__(256) gdn_conv_state_kernel(const VerifyArgs p,
         nw[j] = 0.f;
         if (j < K - 1) {
             const int sp = k - (K - 1) + j;  // sequence position: x row when >= 0
-            nw[j] = sp >= 0 ? ld_in<BF16>(p.x, ((size_t)by * T + sp) * p.C + c) : cs[K - 1 + sp];
+            nw[j] = sp >= 0 ? ld_inc<BF16>(p.x, ((size_t)by * T + sp) * p.C + c, buf_x<BF16 ? 2 : 4>(p), p.dev_status)
+                            : ldfc(cs + (K - 1 + sp), buf_conv(p), p.dev_status);
         }
     }
 #pragma unroll
     for (int j = 0; j < GDN_MAX_CONV_K - 1; ++j)
-        if (j < K - 1) cs[j] = nw[j];
+        if (j < K - 1) stfc(cs + j, nw[j], buf_conv(p), p.dev_status);
 }
 
 }  // namespace

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
 
     int Te = T;  // tokens that count: all for the verify, the accepted k for the commit
     if constexpr (COMMIT) {
-        const int k = accept_len[I.bidx];
+        const int k = ldic(accept_len + I.bidx, buf_accept(p), p.dev_status);
         if (k <= 0 || k > T) {
             if (k != 0 && p.dev_status && tid == 0 && I.y == 0 && I.h == 0 && I.rb == 0)
                 atomicOr(p.dev_status, GDN_DEV_NODE_RANGE);
@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
     prefetch_scalars<BF16, false>(p, I, ga, gb, pr, tid);
     for (int i = tid; i < I.R * U; i += nthreads) {
         const int r = i / U, ug = i - r * U;
-        cp_async16(s0 + swz(kWyRows, r, ug), s_in + (size_t)r * DK + ug * 4);
+        if (GDN_IN(s_in + (size_t)r * DK + ug * 4, 16, buf_state<DK>(p), p.dev_status))
+            cp_async16(s0 + swz(kWyRows, r, ug), s_in + (size_t)r * DK + ug * 4);
     }
     cp_async_commit();
 
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
                     float o = ac_s[t] * h[t];
 #pragma unroll
                     for (int j = 0; j <= t; ++j) o = fmaf(mm_s[t * T + j], u[j], o);
-                    o_row[(size_t)t * p.H_v * p.d_v] = o;
+                    stfc(o_row + (size_t)t * p.H_v * p.d_v, o, buf_out(p), p.dev_status);
                 }
             }
         } else {
@@ -447,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_wy_kernel(const VerifyArgs p,
             const int row = rg + 32 * j;
             if (row < I.R) {
 #pragma unroll
-                for (int m = 0; m < MU; ++m) st4(s_out + (size_t)row * DK + (cg + 8 * m) * 4, acc[j][m]);
+                for (int m = 0; m < MU; ++m)
+                    st4c(s_out + (size_t)row * DK + (cg + 8 * m) * 4, acc[j][m], buf_state<DK>(p), p.dev_status);
             }
         }
     }
@@ -521,6 +523,7 @@ extern "C" int gdn_commit_wy(const gdn_dims *d, int32_t n_tok, const int32_t *ac
     VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_state, conv_state, nullptr, nullptr, nullptr,
                              nullptr, dev_status);
     v.ssm_out = ssm_state;
+    v.accept_len = accept_len_dev;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = dispatch_wy<true>(d, v, accept_len_dev, st);
     if (rc != GDN_OK) return rc;

@@ -70,17 +70,23 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     const int split = blockIdx.x, n = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
     const float *row = logits + ((size_t)b * N + n) * (size_t)V;
+    // buffer extents, for the bounds checks of debug builds (GDN_IN)
+    const size_t B = gridDim.z;
+    const gdndev::Buf bl{logits, B * N * (size_t)V * 4}, bt{tokens, B * N * 4}, bp{parent, B * N * 4},
+        ba{argmax_out, B * N * 4}, bk{accept_len, B * 4}, bn{accept_node, B * 4}, bc{counters, B * 4},
+        br{rowkeys, B * N * 8};
     const int lo = split * chunk;
     const int hi = min(V, lo + chunk);
     // evict-last: the chunk must outlast the previous grid's writes (the
     // verify streams its checkpoints at full bandwidth until it ends)
-    if (lo < hi) gdndev::prefetch_l2_keep_range(row + lo, (size_t)(hi - lo) * 4, tid, kThreads);
+    if (lo < hi && GDN_IN(row + lo, (size_t)(hi - lo) * 4, bl, dev_status))
+        gdndev::prefetch_l2_keep_range(row + lo, (size_t)(hi - lo) * 4, tid, kThreads);
     gdndev::pdl_wait();
     gdndev::pdl_launch_dependents();  // the restore may be scheduled; it waits for this grid
     // the request's draft tokens / parents, loaded now so that the last CTA
     // does not wait for them after the ticket
-    const int my_tok = tid < N ? tokens[(size_t)b * N + tid] : 0;
-    const int my_par = tid < N ? (parent ? parent[(size_t)b * N + tid] : tid - 1) : 0;
+    const int my_tok = tid < N ? gdndev::ldic(tokens + (size_t)b * N + tid, bt, dev_status) : 0;
+    const int my_par = tid < N ? (parent ? gdndev::ldic(parent + (size_t)b * N + tid, bp, dev_status) : tid - 1) : 0;
 
     unsigned long long best = 0ull;  // below every real element
     if ((V & 3) == 0) {
@@ -92,7 +98,9 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
             float4 f[kLoads];
 #pragma unroll
             for (int u = 0; u < kLoads; ++u)
-                if (i0 + u * kThreads < hi4) f[u] = __ldcs(r4 + i0 + u * kThreads);
+                if (i0 + u * kThreads < hi4)
+                    f[u] = GDN_IN(r4 + i0 + u * kThreads, 16, bl, dev_status) ? __ldcs(r4 + i0 + u * kThreads)
+                                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int u = 0; u < kLoads; ++u) {
                 const int i = i0 + u * kThreads;
@@ -106,9 +114,11 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
             }
         }
     } else {
-        for (int i = lo + tid; i < hi; i += kThreads) best = umax64(best, make_key(__ldcs(row + i), (unsigned)i));
+        for (int i = lo + tid; i < hi; i += kThreads)
+            best = umax64(best, make_key(GDN_IN(row + i, 4, bl, dev_status) ? __ldcs(row + i) : 0.f, (unsigned)i));
     }
-    if (lo < hi) gdndev::l2_normal_range(row + lo, (size_t)(hi - lo) * 4, tid, kThreads);  // read: priority back
+    if (lo < hi && GDN_IN(row + lo, (size_t)(hi - lo) * 4, bl, dev_status))
+        gdndev::l2_normal_range(row + lo, (size_t)(hi - lo) * 4, tid, kThreads);  // read: priority back
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, off));
     if ((tid & 31) == 0) red[tid >> 5] = best;
@@ -116,10 +126,12 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     if (tid == 0) {
         for (int w = 1; w < kThreads / 32; ++w) best = umax64(best, red[w]);
         if ((unsigned)(best >> 32) == 0xFFFFFFFFu && dev_status) atomicOr(dev_status, GDN_DEV_NAN_LOGIT);
-        atomicMax(&rowkeys[(size_t)b * N + n], best);  // the row's key: the max over its chunks
+        if (GDN_IN(rowkeys + (size_t)b * N + n, 8, br, dev_status))
+            atomicMax(&rowkeys[(size_t)b * N + n], best);  // the row's key: the max over its chunks
         __threadfence();
-        const unsigned prev = atomicAdd(&counters[b], 1u);
-        is_last = prev == (unsigned)(N * splits - 1);
+        const bool cin = GDN_IN(counters + b, 4, bc, dev_status);
+        const unsigned prev = cin ? atomicAdd(&counters[b], 1u) : 0u;
+        is_last = cin && prev == (unsigned)(N * splits - 1);
     }
     __syncthreads();
     if (!is_last) return;
@@ -128,10 +140,11 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
     // ---- last CTA of request b: every chunk's max has landed in the row keys
     if (tid < N) {  // N <= kMaxNodes <= kThreads
         unsigned long long *kp = rowkeys + (size_t)b * N + tid;
-        const int am = (int)gdndev::key_index(__ldcg(kp));
-        *kp = 0ull;  // leave the workspace zero-filled
+        const bool kin = GDN_IN(kp, 8, br, dev_status);
+        const int am = (int)gdndev::key_index(kin ? __ldcg(kp) : 0ull);
+        if (kin) *kp = 0ull;  // leave the workspace zero-filled
         am_s[tid] = am;
-        argmax_out[(size_t)b * N + tid] = am;
+        if (GDN_IN(argmax_out + (size_t)b * N + tid, 4, ba, dev_status)) argmax_out[(size_t)b * N + tid] = am;
         tok_s[tid] = my_tok;
         // a tree node whose parent is outside [0, i) hangs under the root and
         // never matches, nor does anything below it (flagged below)
@@ -163,9 +176,9 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
                     k = 32 * w + __ffs((int)miss_s[w]) - 2;  // the first mismatching node, minus one
                     break;
                 }
-            accept_len[b] = k;
-            accept_node[b] = k;
-            counters[b] = 0u;  // leave the workspace zero-filled for the next call
+            if (GDN_IN(accept_len + b, 4, bk, dev_status)) accept_len[b] = k;
+            if (GDN_IN(accept_node + b, 4, bn, dev_status)) accept_node[b] = k;
+            if (GDN_IN(counters + b, 4, bc, dev_status)) counters[b] = 0u;  // leave the workspace zero-filled
         }
     } else {
         // every node: its depth and whether its whole root path matches
@@ -192,9 +205,9 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
                 if (ok_s[i] && (dep_s[i] > dep_s[best_node] ||
                                 (dep_s[i] == dep_s[best_node] && path_less(par_s, i, best_node))))
                     best_node = i;
-            accept_len[b] = dep_s[best_node];
-            accept_node[b] = best_node;
-            counters[b] = 0u;
+            if (GDN_IN(accept_len + b, 4, bk, dev_status)) accept_len[b] = dep_s[best_node];
+            if (GDN_IN(accept_node + b, 4, bn, dev_status)) accept_node[b] = best_node;
+            if (GDN_IN(counters + b, 4, bc, dev_status)) counters[b] = 0u;
         }
     }
 }

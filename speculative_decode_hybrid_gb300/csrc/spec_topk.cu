@@ -58,6 +58,10 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *r = logits + (size_t)row * V;
     const int lo = split * chunk, hi = min(V, lo + chunk);
+    // buffer extents, for the bounds checks of debug builds (GDN_IN)
+    const size_t rows = gridDim.y;
+    const gdndev::Buf bl{logits, rows * V * 4}, bi{idx_out, rows * k * 4}, bv{val_out, rows * k * 4},
+        bc{counters, rows * 4}, bk{keys, rows * splits * k * 8};
     gdndev::pdl_wait();
 
     unsigned long long list = 0ull;
@@ -69,7 +73,7 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
         for (int base = a; base < b; base += 32) {
             const int i = base + lane;
             float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < b) f = __ldcs(r4 + i);
+            if (i < b && GDN_IN(r4 + i, 16, bl, dev_status)) f = __ldcs(r4 + i);
             const unsigned e = (unsigned)i * 4u;
             offer(list, i < b ? make_key(f.x, e) : 0ull, k, lane);
             offer(list, i < b ? make_key(f.y, e + 1) : 0ull, k, lane);
@@ -81,7 +85,8 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
         const int a = lo + warp * per, b = min(hi, a + per);
         for (int base = a; base < b; base += 32) {
             const int i = base + lane;
-            offer(list, i < b ? make_key(__ldcs(r + i), (unsigned)i) : 0ull, k, lane);
+            offer(list, i < b ? make_key(GDN_IN(r + i, 4, bl, dev_status) ? __ldcs(r + i) : 0.f, (unsigned)i) : 0ull,
+                  k, lane);
         }
     }
     if (lane < k) lists[warp][lane] = list;
@@ -89,12 +94,14 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
     if (warp == 0) {
         list = lane < k ? lists[0][lane] : 0ull;
         for (int w = 1; w < kWarps; ++w) offer(list, lane < k ? lists[w][lane] : 0ull, k, lane);
-        if (lane < k) keys[((size_t)row * splits + split) * k + lane] = list;
+        if (lane < k && GDN_IN(keys + ((size_t)row * splits + split) * k + lane, 8, bk, dev_status))
+            keys[((size_t)row * splits + split) * k + lane] = list;
         __threadfence();
         unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(&counters[row], 1u);
+        const bool cin = GDN_IN(counters + row, 4, bc, dev_status);
+        if (lane == 0 && cin) prev = atomicAdd(&counters[row], 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (lane == 0) is_last = prev == (unsigned)(splits - 1);
+        if (lane == 0) is_last = cin && prev == (unsigned)(splits - 1);
     }
     __syncthreads();
     if (!is_last || warp != 0) return;
@@ -105,7 +112,7 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
     for (int base = 0; base < splits * k; base += 32) {
         const int i = base + lane;
         unsigned long long c = 0ull;
-        if (i < splits * k) {
+        if (i < splits * k && GDN_IN(kr + i, 8, bk, dev_status)) {
             c = __ldcg(kr + i);
             kr[i] = 0ull;  // leave the workspace zero-filled
         }
@@ -113,11 +120,12 @@ spec_topk_kernel(int V, int k, int splits, int chunk, const float *__restrict__ 
     }
     if (lane < k) {
         const unsigned ix = key_index(list);
-        idx_out[(size_t)row * k + lane] = (int32_t)ix;
-        val_out[(size_t)row * k + lane] = r[ix];
+        if (GDN_IN(idx_out + (size_t)row * k + lane, 4, bi, dev_status)) idx_out[(size_t)row * k + lane] = (int32_t)ix;
+        if (GDN_IN(val_out + (size_t)row * k + lane, 4, bv, dev_status))
+            val_out[(size_t)row * k + lane] = GDN_IN(r + ix, 4, bl, dev_status) ? r[ix] : 0.f;
         if ((unsigned)(list >> 32) == 0xFFFFFFFFu && dev_status) atomicOr(dev_status, GDN_DEV_NAN_LOGIT);
     }
-    if (lane == 0) counters[row] = 0u;  // leave the workspace zero-filled
+    if (lane == 0 && GDN_IN(counters + row, 4, bc, dev_status)) counters[row] = 0u;  // leave the workspace zero-filled
 }
 
 int topk_splits(int rows, int V) {

@@ -14,7 +14,9 @@ import threading
 from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libgdnspec.so")
+# GDNSPEC_LIB selects another build of the library (e.g. the bounds-checking
+# _lib/libgdnspec_debug.so) for the whole process.
+LIB_PATH = os.environ.get("GDNSPEC_LIB") or os.path.join(_HERE, "_lib", "libgdnspec.so")
 
 GDN_F32 = 0
 GDN_BF16 = 1
@@ -40,6 +42,7 @@ GDN_DEV_NAN_LOGIT = 0x2
 GDN_DEV_NODE_RANGE = 0x4
 GDN_DEV_TREE = 0x8
 GDN_DEV_SCHED = 0x10
+GDN_DEV_BOUNDS = 0x20
 
 GDN_MAX_TOKENS = 64
 GDN_MAX_CONV_K = 8
