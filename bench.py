@@ -346,10 +346,8 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         barrier()
         tg1 = time.time()
-        clocks_graph = sampler2.stop(tg0, tg1)
         gstep_ms = [e[0].elapsed_time(e[1]) for e in gev]
         total_max_ms, units_all = aggregate(sum(gstep_ms), units * K, ws, dev)
-        clocks = clocks_graph if clocks_graph.get("samples") else clocks
     else:
         gstep_ms = step_ms
         total_max_ms = eager_max_ms
@@ -382,6 +380,13 @@ def run_ours(args):
     per_layer = None
     if args.commit == "checkpoint" and st.shape.batch == 1 and graph_ok and args.per_layer_steps > 0:
         per_layer = run_per_layer(st, flush, dev, stream, min(K, args.per_layer_steps), units, ws)
+
+    # clocks: sampled from the graph loop to the end of the last timed loop
+    # (graph step, in-graph parts, end to end, per-layer), all under load
+    if graph_ok:
+        clocks_graph = sampler2.stop(tg0, time.time())
+        if clocks_graph.get("samples"):
+            clocks = clocks_graph
 
     # the state moved every step; put the initial one back (not timed)
     st.ssm_state.copy_(ssm0)
