@@ -568,6 +568,10 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
     const size_t gq = (size_t)I.g * DK + lane;            // global q channel of this lane's element 0
     const size_t gk = (size_t)p.H_k * DK + gq;            // and k channel
     const size_t gv = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;  // global channel of v row 0
+    // staged input of window source s (x row >= 0, or -1 - conv-state slot) for local channel c
+    auto win = [&](int s, int c) -> float {
+        return s >= 0 ? ld_in<BF16>(xst, (unsigned)(s * XS + c)) : cstf[(unsigned)(c * (K - 1) + (-1 - s))];
+    };
     for (int t = warp; t < T; t += nwarps) {
         // window position j: x row src[j] >= 0, or conv-state slot -1 - src[j]
         int src[KM];
@@ -602,8 +606,7 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
 #pragma unroll
                     for (int j = 0; j < KM; ++j) {
                         if (j < K) {
-                            const float xv = src[j] >= 0 ? ld_in<BF16>(xst, (size_t)src[j] * XS + c)
-                                                         : cstf[(size_t)c * (K - 1) + (-1 - src[j])];
+                            const float xv = win(src[j], c);
                             a = fmaf(w[j], xv, a);
                             if (cc && j >= 1) stfc(cc + (j - 1), xv, buf_cckpt(p), p.dev_status);
                         }
@@ -614,8 +617,8 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
             const float kq = norm_node<CPL>(acc[0], acc[1], p.q_scale);
 #pragma unroll
             for (int e = 0; e < CPL; ++e) {
-                q_s[(size_t)t * DK + lane + 32 * e] = acc[0][e];
-                k_s[(size_t)t * DK + lane + 32 * e] = acc[1][e];
+                q_s[t * DK + lane + 32 * e] = acc[0][e];
+                k_s[t * DK + lane + 32 * e] = acc[1][e];
             }
             if (lane == 0) kq_s[t] = kq;
         }
@@ -628,13 +631,12 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
 #pragma unroll
             for (int j = 0; j < KM; ++j) {
                 if (j < K) {
-                    const float xv = src[j] >= 0 ? ld_in<BF16>(xst, (size_t)src[j] * XS + c)
-                                                 : cstf[(size_t)c * (K - 1) + (-1 - src[j])];
+                    const float xv = win(src[j], c);
                     acc = fmaf(w[j], xv, acc);
                     if (cv && j >= 1) stfc(cv + (j - 1), xv, buf_cckpt(p), p.dev_status);
                 }
             }
-            v_s[(size_t)t * kRowsPerCta + lc] = silu(acc);
+            v_s[t * kRowsPerCta + lc] = silu(acc);
         }
     }
 }
