@@ -188,6 +188,87 @@ __device__ __forceinline__ void recurrence_step(const VerifyArgs &p, RowState<DK
     }
 }
 
+// The operands of one node's step for this thread's rows: k and q (this
+// lane's columns), the gates, k.q and v of the rows.
+template <int DK, int SL>
+struct StepIn {
+    float4 kk[RowState<DK, SL>::NV4], qq[RowState<DK, SL>::NV4];
+    float at, bt, kqt, vv[SL];
+};
+
+template <int DK, int SL>
+__device__ __forceinline__ void load_step(StepIn<DK, SL> &in, const RowState<DK, SL> &rs, int t, const float *q_s,
+                                          const float *k_s, const float *v_s, const float *a_s, const float *b_s,
+                                          const float *kq_s) {
+    const int j8 = (threadIdx.x & 31) & (kLanesPerRow - 1);
+#pragma unroll
+    for (int m = 0; m < RowState<DK, SL>::NV4; ++m) {
+        in.kk[m] = ld4(k_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+        in.qq[m] = ld4(q_s + (size_t)t * DK + 4 * j8 + kColStride * m);
+    }
+    in.at = a_s[t];
+    in.bt = b_s[t];
+    in.kqt = kq_s[t];
+#pragma unroll
+    for (int s = 0; s < SL; ++s) in.vv[s] = v_s[(size_t)t * kRowsPerCta + rs.lrow[s]];
+}
+
+// recurrence_step with the operands of node t already in `in`; the next
+// node's (tn >= 0) are loaded into `in` as soon as node t's dot products are
+// reduced, ahead of t's checkpoint stores, so that they do not queue behind
+// those stores. The arithmetic is recurrence_step's, operation for operation.
+template <int DK, int SL>
+__device__ __forceinline__ void recurrence_step_ahead(const VerifyArgs &p, RowState<DK, SL> &rs, StepIn<DK, SL> &in,
+                                                      int t, int tn, float *ck0, const float *q_s, const float *k_s,
+                                                      const float *v_s, float *o_s, const float *a_s,
+                                                      const float *b_s, const float *kq_s) {
+    constexpr int NV4 = RowState<DK, SL>::NV4;
+    const int j8 = (threadIdx.x & 31) & (kLanesPerRow - 1);
+    const size_t slot = (size_t)p.H_v * p.d_v * DK;
+    float u[SL], w[SL];
+#pragma unroll
+    for (int s = 0; s < SL; ++s) {
+        u[s] = 0.f;
+        w[s] = 0.f;
+#pragma unroll
+        for (int m = 0; m < NV4; ++m) {
+            u[s] = dot4(rs.S[s][m], in.kk[m], u[s]);
+            w[s] = dot4(rs.S[s][m], in.qq[m], w[s]);
+        }
+    }
+#pragma unroll
+    for (int off = 1; off < kLanesPerRow; off <<= 1) {
+#pragma unroll
+        for (int s = 0; s < SL; ++s) {
+            u[s] += __shfl_xor_sync(0xffffffffu, u[s], off);
+            w[s] += __shfl_xor_sync(0xffffffffu, w[s], off);
+        }
+    }
+    const float at = in.at, bt = in.bt, kqt = in.kqt;
+    float c[SL];
+#pragma unroll
+    for (int s = 0; s < SL; ++s) c[s] = bt * (in.vv[s] - at * u[s]);
+    float4 kk[NV4];
+#pragma unroll
+    for (int m = 0; m < NV4; ++m) kk[m] = in.kk[m];
+    if (tn >= 0) load_step(in, rs, tn, q_s, k_s, v_s, a_s, b_s, kq_s);
+    float *ck = ck0 + (size_t)t * slot;
+#pragma unroll
+    for (int s = 0; s < SL; ++s) {
+#pragma unroll
+        for (int m = 0; m < NV4; ++m) {
+            float4 n;
+            n.x = fmaf(c[s], kk[m].x, at * rs.S[s][m].x);
+            n.y = fmaf(c[s], kk[m].y, at * rs.S[s][m].y);
+            n.z = fmaf(c[s], kk[m].z, at * rs.S[s][m].z);
+            n.w = fmaf(c[s], kk[m].w, at * rs.S[s][m].w);
+            rs.S[s][m] = n;
+            if (p.ssm_ckpt) st4c(ck + (size_t)rs.lrow[s] * DK + 4 * j8 + kColStride * m, n, buf_ckpt<DK>(p), p.dev_status);
+        }
+        if (j8 == 0) o_s[(size_t)t * kRowsPerCta + rs.lrow[s]] = fmaf(c[s], kqt, at * w[s]);
+    }
+}
+
 // The recurrence over all nodes of one item. Trees run the nodes in the
 // depth-first order of the tree tables and follow their reload plan: a
 // node whose parent is not the node just computed takes the parent's state
@@ -231,6 +312,15 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL>
                 if (park >= 0) park_rows(rs, tmem, park);
             }
         }
+    } else if constexpr (SL <= 2) {
+        // few rows per thread leave registers for the next node's operands
+        // (not in the tree loop: measured slower there, where parks and
+        // reloads sit between the steps)
+        StepIn<DK, SL> in;
+        if (p.T > 0) load_step(in, rs, 0, q_s, k_s, v_s, a_s, b_s, kq_s);
+        for (int t = 0; t < p.T; ++t)
+            recurrence_step_ahead<DK, SL>(p, rs, in, t, t + 1 < p.T ? t + 1 : -1, ck0, q_s, k_s, v_s, o_s, a_s, b_s,
+                                          kq_s);
     } else {
         for (int t = 0; t < p.T; ++t) recurrence_step<DK, SL>(p, rs, t, ck0, q_s, k_s, v_s, o_s, a_s, b_s, kq_s);
     }

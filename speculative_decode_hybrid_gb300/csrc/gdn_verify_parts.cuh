@@ -521,6 +521,118 @@ __device__ __forceinline__ void load_taps(const unsigned char *wst, int c, int K
     }
 }
 
+// What every node of an item's conv prologue shares.
+struct ConvCtx {
+    const unsigned char *xst, *wst;  // staged x tile and conv taps
+    const float *cstf;               // staged conv state
+    float *q_s, *k_s, *v_s, *kq_s;   // outputs in shared memory
+    float *cck;                      // this request's conv checkpoints (or null)
+    size_t cc_tok, gq, gk, gv;       // checkpoint floats per node; global q, k channel of element 0, v row 0
+    unsigned qk_own;                 // q/k channel groups whose conv checkpoints this item writes
+    int K, lane;
+    bool skip_qk;
+};
+
+// Window position j of a node: x row s >= 0 or conv-state slot -1 - s of
+// local channel c. AX: the caller knows s >= 0 (no branch).
+template <bool BF16, bool AX, int XS>
+__device__ __forceinline__ float win_at(const ConvCtx &x, int s, int c) {
+    if constexpr (AX) return ld_in<BF16>(x.xst, (unsigned)(s * XS + c));
+    else
+        return s >= 0 ? ld_in<BF16>(x.xst, (unsigned)(s * XS + c)) : x.cstf[(unsigned)(c * (x.K - 1) + (-1 - s))];
+}
+
+// conv1d + SiLU of one node t (window sources src), the q/k norms and k.q.
+// AX: every window position is an x row (every chain node from K - 1 on):
+// the loads of all the node's channels can then issue before the first use.
+// QK / V: the q/k half (with the norms) and the v half of the node.
+template <int DK, bool BF16, int KT, int KM, bool AX, bool QK, bool V>
+__device__ __forceinline__ void conv_node(const VerifyArgs &p, const Item &I, const ConvCtx &x, int t,
+                                          const int (&src)[KM]) {
+    constexpr int XS = 2 * DK + kRowsPerCta;
+    constexpr int CPL = DK / 32;
+    const int K = KT > 0 ? KT : x.K, lane = x.lane;
+    if (QK && !x.skip_qk) {
+        // q (half 0) and k (half 1): element e is channel lane + 32 e
+        float acc[2][CPL];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) {
+                const int c = hf * DK + lane + 32 * e;  // local channel
+                float w[KM];
+                load_taps<BF16, KT, KM>(x.wst, c, K, w);
+                float *cc = (x.qk_own >> (hf * CPL + e)) & 1u
+                                ? x.cck + (size_t)t * x.cc_tok + ((hf ? x.gk : x.gq) + 32 * e) * (K - 1)
+                                : nullptr;
+                float a = 0.f;
+#pragma unroll
+                for (int j = 0; j < KM; ++j) {
+                    if (j < K) {
+                        const float xv = win_at<BF16, AX, XS>(x, src[j], c);
+                        a = fmaf(w[j], xv, a);
+                        if (cc && j >= 1) stfc(cc + (j - 1), xv, buf_cckpt(p), p.dev_status);
+                    }
+                }
+                acc[hf][e] = silu(a);
+            }
+        }
+        const float kq = norm_node<CPL>(acc[0], acc[1], p.q_scale);
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) {
+            x.q_s[t * DK + lane + 32 * e] = acc[0][e];
+            x.k_s[t * DK + lane + 32 * e] = acc[1][e];
+        }
+        if (lane == 0) x.kq_s[t] = kq;
+    }
+    if constexpr (!V) return;
+    for (int lc = lane; lc < I.R; lc += 32) {
+        const int c = 2 * DK + lc;
+        float w[KM];
+        load_taps<BF16, KT, KM>(x.wst, c, K, w);
+        float *cv = x.cck ? x.cck + (size_t)t * x.cc_tok + (x.gv + lc) * (K - 1) : nullptr;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j < K) {
+                const float xv = win_at<BF16, AX, XS>(x, src[j], c);
+                acc = fmaf(w[j], xv, acc);
+                if (cv && j >= 1) stfc(cv + (j - 1), xv, buf_cckpt(p), p.dev_status);
+            }
+        }
+        x.v_s[t * kRowsPerCta + lc] = silu(acc);
+    }
+}
+
+// Node t: its window sources (x row >= 0, or -1 - conv-state slot), then
+// conv_node, branch-free when the whole window is in x (chains).
+template <int DK, bool BF16, bool TREE, int KT, int KM, bool QK, bool V>
+__device__ __forceinline__ void conv_at(const VerifyArgs &p, const Item &I, const ConvCtx &x, int t,
+                                        const int *src_s) {
+    const int K = KT > 0 ? KT : x.K;
+    int src[KM];
+    bool all_x = true;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        int s = 0;
+        if (j < K) {
+            if constexpr (TREE) {
+                const int sn = src_s[t * K + j];  // >= 1: node; else -1 - slot
+                s = sn >= 1 ? sn - 1 : sn;
+            } else {
+                const int sp = t - (K - 1) + j;
+                s = sp >= 0 ? sp : -1 - (K - 1 + sp);
+            }
+            all_x = all_x && s >= 0;
+        }
+        src[j] = s;
+    }
+    if (!TREE && all_x)  // the same for the whole warp (chains: measured slower for trees)
+        conv_node<DK, BF16, KT, KM, true, QK, V>(p, I, x, t, src);
+    else
+        conv_node<DK, BF16, KT, KM, false, QK, V>(p, I, x, t, src);
+}
+
 // conv1d + SiLU of item I from its staged inputs, fused with the q/k L2
 // norms: one warp per node. Lane l owns q and k channels l, l + 32, ... of
 // the key head (d_k / 32 each) and v channels l, l + 32, ... of the item, so
@@ -545,13 +657,19 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
                                                  const unsigned char *wst, const unsigned char *cst,
                                                  const int *src_s, float *q_s, float *k_s, float *v_s,
                                                  float *kq_s, bool skip_qk, int warp, int nwarps) {
-    constexpr int XS = 2 * DK + kRowsPerCta;
     constexpr int CPL = DK / 32;
     constexpr int KM = KT > 0 ? KT : GDN_MAX_CONV_K;
     const int T = p.T, K = KT > 0 ? KT : p.K;
     const int lane = threadIdx.x & 31;
-    const float *cstf = reinterpret_cast<const float *>(cst);
-    const size_t cc_tok = (size_t)p.C * (K - 1);
+    ConvCtx x;
+    x.xst = xst;
+    x.wst = wst;
+    x.cstf = reinterpret_cast<const float *>(cst);
+    x.q_s = q_s;
+    x.k_s = k_s;
+    x.v_s = v_s;
+    x.kq_s = kq_s;
+    x.cc_tok = (size_t)p.C * (K - 1);
     const bool ckpt = p.conv_ckpt != nullptr;
     // q/k channel groups whose conv checkpoints this item writes (bit hf * CPL + e)
     unsigned qk_own = 0;
@@ -564,81 +682,15 @@ __device__ __forceinline__ void conv_norm_staged(const VerifyArgs &p, const Item
             qk_own = (1u << (2 * CPL)) - 1u;
         }
     }
-    float *cck = ckpt ? p.conv_ckpt + (size_t)I.by * T * cc_tok : nullptr;
-    const size_t gq = (size_t)I.g * DK + lane;            // global q channel of this lane's element 0
-    const size_t gk = (size_t)p.H_k * DK + gq;            // and k channel
-    const size_t gv = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;  // global channel of v row 0
-    // staged input of window source s (x row >= 0, or -1 - conv-state slot) for local channel c
-    auto win = [&](int s, int c) -> float {
-        return s >= 0 ? ld_in<BF16>(xst, (unsigned)(s * XS + c)) : cstf[(unsigned)(c * (K - 1) + (-1 - s))];
-    };
-    for (int t = warp; t < T; t += nwarps) {
-        // window position j: x row src[j] >= 0, or conv-state slot -1 - src[j]
-        int src[KM];
-#pragma unroll
-        for (int j = 0; j < KM; ++j) {
-            int s = 0;
-            if (j < K) {
-                if constexpr (TREE) {
-                    const int sn = src_s[t * K + j];  // >= 1: node; else -1 - slot
-                    s = sn >= 1 ? sn - 1 : sn;
-                } else {
-                    const int sp = t - (K - 1) + j;
-                    s = sp >= 0 ? sp : -1 - (K - 1 + sp);
-                }
-            }
-            src[j] = s;
-        }
-        if (!skip_qk) {
-            // q (half 0) and k (half 1): element e is channel lane + 32 e
-            float acc[2][CPL];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                for (int e = 0; e < CPL; ++e) {
-                    const int c = hf * DK + lane + 32 * e;  // local channel
-                    float w[KM];
-                    load_taps<BF16, KT, KM>(wst, c, K, w);
-                    float *cc = (qk_own >> (hf * CPL + e)) & 1u
-                                    ? cck + (size_t)t * cc_tok + ((hf ? gk : gq) + 32 * e) * (K - 1)
-                                    : nullptr;
-                    float a = 0.f;
-#pragma unroll
-                    for (int j = 0; j < KM; ++j) {
-                        if (j < K) {
-                            const float xv = win(src[j], c);
-                            a = fmaf(w[j], xv, a);
-                            if (cc && j >= 1) stfc(cc + (j - 1), xv, buf_cckpt(p), p.dev_status);
-                        }
-                    }
-                    acc[hf][e] = silu(a);
-                }
-            }
-            const float kq = norm_node<CPL>(acc[0], acc[1], p.q_scale);
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) {
-                q_s[t * DK + lane + 32 * e] = acc[0][e];
-                k_s[t * DK + lane + 32 * e] = acc[1][e];
-            }
-            if (lane == 0) kq_s[t] = kq;
-        }
-        for (int lc = lane; lc < I.R; lc += 32) {
-            const int c = 2 * DK + lc;
-            float w[KM];
-            load_taps<BF16, KT, KM>(wst, c, K, w);
-            float *cv = ckpt ? cck + (size_t)t * cc_tok + (gv + lc) * (K - 1) : nullptr;
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < KM; ++j) {
-                if (j < K) {
-                    const float xv = win(src[j], c);
-                    acc = fmaf(w[j], xv, acc);
-                    if (cv && j >= 1) stfc(cv + (j - 1), xv, buf_cckpt(p), p.dev_status);
-                }
-            }
-            v_s[t * kRowsPerCta + lc] = silu(acc);
-        }
-    }
+    x.qk_own = qk_own;
+    x.cck = ckpt ? p.conv_ckpt + (size_t)I.by * T * x.cc_tok : nullptr;
+    x.gq = (size_t)I.g * DK + lane;                                   // global q channel of this lane's element 0
+    x.gk = (size_t)p.H_k * DK + x.gq;                                 // and k channel
+    x.gv = 2 * (size_t)p.H_k * DK + (size_t)I.h * p.d_v + I.row0;     // global channel of v row 0
+    x.K = K;
+    x.lane = lane;
+    x.skip_qk = skip_qk;
+    for (int t = warp; t < T; t += nwarps) conv_at<DK, BF16, TREE, KT, KM, true, true>(p, I, x, t, src_s);
 }
 
 // Warm L2 with item I's inputs: its state rows, x tile (all p.T nodes), conv
