@@ -306,37 +306,38 @@ __device__ __forceinline__ void tree_tables(const VerifyArgs &p, const int32_t *
 
 // L2 norms of one node's q and k, held by one warp: lane l holds elements
 // l, l + 32, ..., l + 32 (CPL - 1) of each. u / sqrt(sum u^2 + 1e-6) in place, q
-// also scaled by q_scale; returns k.q (the same value in every lane: each
-// xor-butterfly stage adds the same two operands in both partner lanes).
-// Every kernel normalises through this function, so the bytes of q and k
-// do not depend on which kernel computed them.
+// also scaled by q_scale; returns k.q of the normalised vectors, computed as
+// (sum q k) iq q_scale ik from the raw q.k, reduced in the same butterfly as
+// the two sums of squares (one chain of shuffles per node, not two). Every
+// value is the same in every lane: each xor-butterfly stage adds the same
+// two operands in both partner lanes. Every kernel normalises through this
+// function, so the bytes of q, k and k.q do not depend on which kernel
+// computed them.
 template <int CPL>
 __device__ __forceinline__ float norm_node(float (&qv)[CPL], float (&kv)[CPL], float q_scale) {
-    float sq = 0.f, sk = 0.f;
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
     for (int e = 0; e < CPL; ++e) {
         sq = fmaf(qv[e], qv[e], sq);
         sk = fmaf(kv[e], kv[e], sk);
+        sqk = fmaf(qv[e], kv[e], sqk);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         sq += __shfl_xor_sync(0xffffffffu, sq, off);
         sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
     }
     // the hardware reciprocal square root (a few ulp), far inside the 2e-3
     // tolerance of the states and outputs
     const float iq = rsqrtf(sq + 1e-6f);
     const float ik = rsqrtf(sk + 1e-6f);
-    float kq = 0.f;
 #pragma unroll
     for (int e = 0; e < CPL; ++e) {
         qv[e] = qv[e] * iq * q_scale;
         kv[e] = kv[e] * ik;
-        kq = fmaf(qv[e], kv[e], kq);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-    return kq;
+    return sqk * iq * q_scale * ik;
 }
 
 // Per-head L2 norm of q and k (already convolved, in shared memory), q scale,
