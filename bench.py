@@ -368,7 +368,7 @@ def run_ours(args):
     #      verify -> accept, beside the whole step
     parts = None
     if graph_ok and rank == 0:
-        parts = graph_part_costs(st, args.commit, f_verify, flush, dev, stream, min(K, 50))
+        parts = graph_part_costs(st, args.commit, f_verify, flush, dev, stream, min(K, 200))
 
     # ---- end to end through the public API, host buffers, copies timed
     e2e = None
@@ -484,22 +484,27 @@ def graph_part_costs(st, commit, f_verify, flush, dev, stream, n):
            "step": lambda stream=None: (f_verify(stream), st.accept(stream), f_commit(stream))}
     out = {}
     try:
+        graphs = {}
         for name, fn in fns.items():
             st.step_fn = lambda c, fn=fn: fn
-            g = st.capture(name)
+            graphs[name] = st.capture(name)
             for _ in range(3):
-                g.replay()
-            torch.cuda.synchronize(dev)
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-            for i in range(n):
+                graphs[name].replay()
+        torch.cuda.synchronize(dev)
+        # the four graphs replayed in turn, so that a drift of the box's
+        # speed during the loop weighs on all of them alike
+        ev = {name: [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)] for name in graphs}
+        for i in range(n):
+            for name, g in graphs.items():
                 flush.fill_(i & 0xFF)
-                ev[i][0].record(stream)
+                ev[name][i][0].record(stream)
                 g.replay()
-                ev[i][1].record(stream)
-            torch.cuda.synchronize(dev)
-            out[name] = statistics.median([a.elapsed_time(b) for a, b in ev]) * 1e3
-            st.ssm_state.copy_(ssm0)
-            st.conv_state.copy_(conv0)
+                ev[name][i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        for name in graphs:
+            out[name] = statistics.median([a.elapsed_time(b) for a, b in ev[name]]) * 1e3
+        st.ssm_state.copy_(ssm0)
+        st.conv_state.copy_(conv0)
     finally:
         st.__dict__.pop("step_fn", None)  # the class's step_fn again
         st._graph = main_graph

@@ -16,7 +16,7 @@
 //    streams its writes until then) and sets it back to normal once read.
 //  * The CTA folds its key into its row's key in the caller's workspace
 //    (a 64-bit atomic max in L2) and bumps a per-request arrival counter.
-//    The last CTA of a request (threadfence + atomic counter, no spinning)
+//    The last CTA of a request (an acquire-release atomic counter, no spinning)
 //    reads the N row keys (one thread each), writes argmax_out, and decides
 //    the acceptance in parallel: a chain's accepted length is the number of
 //    leading matches (a warp ballot of the mismatches); a tree's nodes find
@@ -128,14 +128,16 @@ spec_accept_kernel(int N, int V, int splits, int chunk, const float *__restrict_
         if ((unsigned)(best >> 32) == 0xFFFFFFFFu && dev_status) atomicOr(dev_status, GDN_DEV_NAN_LOGIT);
         if (GDN_IN(rowkeys + (size_t)b * N + n, 8, br, dev_status))
             atomicMax(&rowkeys[(size_t)b * N + n], best);  // the row's key: the max over its chunks
-        __threadfence();
+        // the ticket: release orders this CTA's key fold before it, acquire
+        // orders the last CTA's reads of every row key after it
         const bool cin = GDN_IN(counters + b, 4, bc, dev_status);
-        const unsigned prev = cin ? atomicAdd(&counters[b], 1u) : 0u;
+        unsigned prev = 0u;
+        if (cin)
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(counters + b) : "memory");
         is_last = cin && prev == (unsigned)(N * splits - 1);
     }
     __syncthreads();
     if (!is_last) return;
-    __threadfence();
 
     // ---- last CTA of request b: every chunk's max has landed in the row keys
     if (tid < N) {  // N <= kMaxNodes <= kThreads
