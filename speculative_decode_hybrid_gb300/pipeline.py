@@ -53,9 +53,12 @@ class SpecStep:
         self.tokens = _dev(wl.tokens, dev)
         self.parent_host = wl.parent
         self.parent = _dev(wl.parent, dev) if self.tree else None
-        self.argmax = torch.zeros((B, s.n_nodes), dtype=torch.int32, device=dev)
-        self.accept_len = torch.zeros((B,), dtype=torch.int32, device=dev)
-        self.accept_node = torch.zeros((B,), dtype=torch.int32, device=dev)
+        # the step's result, one buffer [accept_len (B) | accept_node (B) |
+        # argmax (B x nodes)] so that it goes back to the host in one copy
+        self.result = torch.zeros((2 * B + B * s.n_nodes,), dtype=torch.int32, device=dev)
+        self.accept_len = self.result[:B]
+        self.accept_node = self.result[B:2 * B]
+        self.argmax = self.result[2 * B:].view(B, s.n_nodes)
         self.ws_bytes = G.spec_accept_workspace_bytes(B, s.n_nodes)
         self.workspace = torch.zeros((self.ws_bytes,), dtype=torch.uint8, device=dev)
         self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
@@ -265,6 +268,23 @@ class SpecStep:
         """One captured step on the current stream (capture() first)."""
         self._graph.replay()
 
+    def host_result_buffers(self) -> dict:
+        """Pinned host buffers for the step's result, laid out like the device
+        result buffer: "accept_len", "accept_node" and "argmax" are views of
+        "_packed", which run_host_step and capture_host_step copy back in one
+        piece (a dict without "_packed" gets one copy per tensor)."""
+        packed = torch.empty(self.result.shape, dtype=torch.int32).pin_memory()
+        B = self.accept_len.numel()
+        return {"_packed": packed, "accept_len": packed[:B], "accept_node": packed[B:2 * B],
+                "argmax": packed[2 * B:].view(self.argmax.shape)}
+
+    def _copy_result(self, out_host: dict):
+        if "_packed" in out_host:
+            out_host["_packed"].copy_(self.result, non_blocking=True)
+        else:
+            for name in ("accept_len", "accept_node", "argmax"):
+                out_host[name].copy_(getattr(self, name), non_blocking=True)
+
     def capture_host_step(self, host: dict, out_host: dict, commit: str = "checkpoint", chunks=(1, 3, 8)):
         """Capture the end-to-end step for fixed pinned host buffers (see
         run_host_step) into one CUDA graph that pipelines the host link with
@@ -323,8 +343,7 @@ class SpecStep:
             main.wait_event(copied)
             self.accept(stream=main)
             finish(stream=main)
-            for name in ("accept_len", "accept_node", "argmax"):
-                out_host[name].copy_(getattr(self, name), non_blocking=True)
+            self._copy_result(out_host)
         torch.cuda.current_stream(self.device).wait_stream(main)
         self._graph_host = g
         self._graph_host_bufs = (host, out_host)
@@ -384,7 +403,8 @@ def pinned_host_inputs(wl: Workload):
 def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None, graph: bool = False):
     """End-to-end step through the public API: H2D copy of the step's inputs
     from pinned memory, verify -> accept -> commit, D2H copy of the result
-    (accept_len, accept_node, argmax). With graph=True the step is one graph
+    (accept_len, accept_node, argmax: one copy when out_host comes from
+    SpecStep.host_result_buffers). With graph=True the step is one graph
     launch: the whole host step captured by capture_host_step for these
     buffers, else the captured device step between eager copies. Returns
     (h2d_bytes, d2h_bytes)."""
@@ -403,6 +423,5 @@ def run_host_step(st: SpecStep, host: dict, out_host: dict, stream=None, graph: 
         st.replay()
     else:
         st.step_fn(getattr(st, "commit", "checkpoint"))(stream)
-    for name in ("accept_len", "accept_node", "argmax"):
-        out_host[name].copy_(getattr(st, name), non_blocking=True)
+    st._copy_result(out_host)
     return h2d, d2h

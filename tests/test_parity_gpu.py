@@ -502,6 +502,14 @@ def test_host_buffer_step_matches_device_step():
     am, kl, kn = oracle.accept_greedy(wl.logits[0], wl.tokens[0])
     assert int(out["accept_len"][0]) == kl == 2 and int(out["accept_node"][0]) == kn
     np.testing.assert_array_equal(out["argmax"][0].numpy(), am)
+    # the packed result buffer comes back in one copy with the same values
+    packed = st.host_result_buffers()
+    packed["_packed"].fill_(-1)
+    _, d2h_p = run_host_step(st, host, packed)
+    torch.cuda.synchronize()
+    assert d2h_p == d2h
+    assert int(packed["accept_len"][0]) == kl and int(packed["accept_node"][0]) == kn
+    np.testing.assert_array_equal(packed["argmax"][0].numpy(), am)
 
 
 @pytest.mark.parametrize("wid,commit", [(2, "checkpoint"), (3, "checkpoint"), (2, "replay"), (2, "wy")])
@@ -520,7 +528,9 @@ def test_host_step_graph_equals_eager_host_steps(wid, commit):
 
     eager, graph = SpecStep(wl), SpecStep(wl)
     eager.commit = commit
-    out_e, out_g = outs(), outs()
+    # the eager side copies each result tensor back, the graph side the one
+    # packed result buffer (host_result_buffers)
+    out_e, out_g = outs(), graph.host_result_buffers()
     for _ in range(3):  # the capture runs one eager host step first
         run_host_step(eager, host, out_e)
     graph.capture_host_step(host, out_g, commit)
