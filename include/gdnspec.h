@@ -89,8 +89,9 @@ typedef void *gdn_stream_t;
                                      used parent i-1 for that node (verify) or left it unmatched
                                      (acceptance) instead of reading out of bounds */
 #define GDN_DEV_SCHED 0x10        /* verify: a CTA gave up waiting for an asynchronous hardware
-                                     operation (the answer to a work-stealing request, or a
-                                     tensor-core product); its outputs are incomplete */
+                                     operation (the answer to a work-stealing request, a
+                                     tensor-core product, or (the _pipelined calls) an input
+                                     flag); its outputs are incomplete */
 #define GDN_DEV_BOUNDS 0x20       /* debug builds of the library only (GDN_DEBUG_BOUNDS): a kernel
                                      skipped a global access that fell outside its buffer */
 
@@ -207,6 +208,44 @@ int gdn_tree_verify_ex(const gdn_dims *dims, int32_t n_nodes,
                        const float *ssm_in, const float *conv_in,
                        float *ssm_ckpt, float *conv_ckpt, float *out,
                        int32_t *dev_status, uint32_t flags, gdn_stream_t stream);
+
+/*
+ * gdn_verify_span_pipelined / gdn_tree_verify_pipelined — the _ex calls (the
+ * same operation, the same bytes) for inputs that are still landing when the
+ * kernel starts: a step whose x, a and b arrive over the host link while
+ * the verify already runs the layers that are there. This is an interface
+ * of this library, not of the pages.
+ *
+ *   x_ready [B][layers] int32, device memory, nullable (null: the _ex call).
+ *           The kernel reads the x, a and b rows of (request b, layer y) only
+ *           after x_ready[b * layers + y] != 0. It waits for that (bounded,
+ *           about a quarter second; a wait that gives up sets GDN_DEV_SCHED in
+ *           *dev_status and the item reads whatever is there). Everything
+ *           else (ssm_in, conv_in, conv_w, parent_dev) must be in place when
+ *           the call's kernel starts, as for the _ex calls.
+ *           The caller sets a flag only after that (request, layer)'s rows
+ *           have landed, with a copy-engine write queued behind them (a
+ *           host-to-device cudaMemcpyAsync on the stream that copied the
+ *           rows), never from a kernel: a kernel could be waiting for an SM
+ *           that this launch holds. The kernel reads the flags and never
+ *           clears them: the caller zeroes them before the next call's
+ *           copies set them again.
+ * Returns as the _ex calls, and GDN_ERR_ALIGN for an x_ready not 4-byte
+ * aligned.
+ */
+int gdn_verify_span_pipelined(const gdn_dims *dims, int32_t n_tok,
+                              const void *x, const void *a, const void *b, const void *conv_w,
+                              const float *ssm_in, const float *conv_in,
+                              float *ssm_ckpt, float *conv_ckpt, float *out,
+                              int32_t *dev_status, uint32_t flags, const int32_t *x_ready,
+                              gdn_stream_t stream);
+int gdn_tree_verify_pipelined(const gdn_dims *dims, int32_t n_nodes,
+                              const int32_t *parent_host, const int32_t *parent_dev,
+                              const void *x, const void *a, const void *b, const void *conv_w,
+                              const float *ssm_in, const float *conv_in,
+                              float *ssm_ckpt, float *conv_ckpt, float *out,
+                              int32_t *dev_status, uint32_t flags, const int32_t *x_ready,
+                              gdn_stream_t stream);
 
 /*
  * spec_accept_greedy — greedy acceptance for a batch of requests.

@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_kernel(const VerifyArg
     const Item I = decode_item(p, (blockIdx.z * p.H_v + blockIdx.y) * nrb + blockIdx.x, nrb);
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5;
     const void *__restrict__ xin = p.x;
+    wait_ready(p, I.by);  // inputs landing during the launch: this item's x, a, b rows
 
     // the initial state of this thread's rows, loaded first so that its
     // latency overlaps the prologue below
@@ -518,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     // work stealing: this CTA's own item first, then items of cancelled CTAs
     __shared__ __align__(16) unsigned long long steal_s[3];  // response (16 B), mbarrier
     __shared__ int next_s;
+    __shared__ int next_ready_s;  // the next item's inputs have landed (x_ready), or need no wait
     __shared__ unsigned park_s;  // tensor-memory columns of the parked branch points (trees)
     // Tree branch points are parked in tensor memory: 2 states of 16 rows
     // per warp (2 x 128 columns at d_k = 128, half of the SM's 512 for each
@@ -577,6 +579,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
     };
     VerifyArgs pn = p;  // p with T = the staged item's tokens
     pn.T = tokens_of(I0);
+    // Inputs landing during the launch (x_ready): compiled into the full-size
+    // instantiations only; the host never picks the 4-rows-per-warp one for a
+    // call with x_ready (its code stays as it is without the wait).
+    constexpr bool kReady = SL == kSlots;
+    if constexpr (kReady) wait_ready(p, I0.by);  // the first item's x, a, b rows
     prefetch_item<DK, BF16>(p, I0, xst, wst, cst, true, tid, nthreads, pn.T, early ? kStageX : kStageAll);
     prefetch_scalars<BF16, TREE>(p, I0, ga, gb, pr, tid);
     while (true) {
@@ -625,18 +632,31 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
                 if (nx < 0 || nx >= n_items) stealing = false;
             }
             next_s = nx;
+            // inputs landing during the launch: whether the next item's rows
+            // are there already (the acquire here and the barrier below order
+            // every thread's staging reads after the flag)
+            if constexpr (kReady) {
+                next_ready_s = 1;
+                if (p.x_ready && nx >= 0 && nx < n_items) next_ready_s = ready_flag(p, decode_item(p, nx, nrb).by);
+            }
         }
         __syncthreads();  // staging consumed; q, k (normalised), k.q, v ready; next_s set
 
         const int next = next_s >= 0 && next_s < n_items ? next_s : n_items;
         if (next >= n_items) pdl_launch_dependents();  // nothing left to take: this CTA's last item
         bool next_reuse = false;
+        // the next item's inputs are staged during this item's recurrence,
+        // unless they have not landed yet (x_ready): then after it
+        const bool stage_now = !kReady || next_ready_s != 0;
+        Item In{};
         if (next < n_items) {
-            const Item In = decode_item(p, next, nrb);
+            In = decode_item(p, next, nrb);
             next_reuse = In.by == I.by && In.g == I.g;
             pn.T = tokens_of(In);
-            prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads, pn.T);
-            prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
+            if (stage_now) {
+                prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads, pn.T);
+                prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
+            }
         }
         if (has_rows) {
             float *ck0 =
@@ -656,6 +676,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_verify_persistent(const Verif
         __syncthreads();
         if constexpr (!RP) write_out(p, I, o_s, threadIdx.x, blockDim.x);
         if (next >= n_items) break;
+        if (kReady && !stage_now) {
+            wait_ready(p, In.by);
+            prefetch_item<DK, BF16>(p, In, xst, wst, cst, !next_reuse, tid, nthreads, pn.T);
+            prefetch_scalars<BF16, TREE>(p, In, ga, gb, pr, tid);
+        }
         it = next;
         reuse_qk = next_reuse;
     }
@@ -784,7 +809,7 @@ int launch_verify(const VerifyArgs &a, int batch, bool aligned_inputs, cudaStrea
         const long long want = 2LL * (sms > 0 ? sms : 152);
         const int min_rpi = a.K == 4 ? 32 : kRowsPerWarp;
         while (pa.rpi > min_rpi && (long long)batch * a.Y * a.H_v * row_blocks(pa) < want) pa.rpi /= 2;
-        const bool small = pa.rpi <= 32 && a.K == 4;
+        const bool small = pa.rpi <= 32 && a.K == 4 && !a.x_ready;  // (x_ready: full-size instantiations)
         // with 4 rows per warp an item of rpi rows needs rpi / 4 warps
         const int thr = small && threads < pa.rpi / kRowsPerSlot * 32 ? pa.rpi / kRowsPerSlot * 32 : threads;
         auto kern = small ? gdn_verify_persistent<DK, BF16, TREE, 4, 1>
@@ -868,18 +893,29 @@ int check_common(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
 
 }  // namespace
 
-extern "C" int gdn_verify_span_ex(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
-                                  const void *b, const void *conv_w, const float *ssm_in,
-                                  const float *conv_in, float *ssm_ckpt, float *conv_ckpt, float *out,
-                                  int32_t *dev_status, uint32_t flags, gdn_stream_t stream) {
+extern "C" int gdn_verify_span_pipelined(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
+                                         const void *b, const void *conv_w, const float *ssm_in,
+                                         const float *conv_in, float *ssm_ckpt, float *conv_ckpt, float *out,
+                                         int32_t *dev_status, uint32_t flags, const int32_t *x_ready,
+                                         gdn_stream_t stream) {
     int rc = check_common(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out);
     if (rc != GDN_OK) return rc;
     if (flags & ~(uint32_t)GDN_VERIFY_STATE_READY) return GDN_ERR_FLAGS;
     if (dev_status && !gdnhost::aligned_to(dev_status, 4)) return GDN_ERR_ALIGN;
+    if (x_ready && !gdnhost::aligned_to(x_ready, 4)) return GDN_ERR_ALIGN;
     VerifyArgs v = make_args(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out, nullptr,
                              dev_status);
     v.early = (flags & GDN_VERIFY_STATE_READY) ? 1 : 0;
+    v.x_ready = x_ready;
     return dispatch_verify<false>(d, v, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_verify_span_ex(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
+                                  const void *b, const void *conv_w, const float *ssm_in,
+                                  const float *conv_in, float *ssm_ckpt, float *conv_ckpt, float *out,
+                                  int32_t *dev_status, uint32_t flags, gdn_stream_t stream) {
+    return gdn_verify_span_pipelined(d, n_tok, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out,
+                                     dev_status, flags, nullptr, stream);
 }
 
 extern "C" int gdn_verify_span(const gdn_dims *d, int32_t n_tok, const void *x, const void *a,
@@ -904,6 +940,16 @@ extern "C" int gdn_tree_verify_ex(const gdn_dims *d, int32_t n_nodes, const int3
                                   const void *b, const void *conv_w, const float *ssm_in,
                                   const float *conv_in, float *ssm_ckpt, float *conv_ckpt,
                                   float *out, int32_t *dev_status, uint32_t flags, gdn_stream_t stream) {
+    return gdn_tree_verify_pipelined(d, n_nodes, parent_host, parent_dev, x, a, b, conv_w, ssm_in, conv_in,
+                                     ssm_ckpt, conv_ckpt, out, dev_status, flags, nullptr, stream);
+}
+
+extern "C" int gdn_tree_verify_pipelined(const gdn_dims *d, int32_t n_nodes, const int32_t *parent_host,
+                                         const int32_t *parent_dev, const void *x, const void *a,
+                                         const void *b, const void *conv_w, const float *ssm_in,
+                                         const float *conv_in, float *ssm_ckpt, float *conv_ckpt,
+                                         float *out, int32_t *dev_status, uint32_t flags,
+                                         const int32_t *x_ready, gdn_stream_t stream) {
     if (!d) return GDN_ERR_NULL;
     if (n_nodes < 2) return GDN_ERR_TREE_TRUNCATED;
     int rc = check_common(d, n_nodes - 1, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out);
@@ -914,9 +960,11 @@ extern "C" int gdn_tree_verify_ex(const gdn_dims *d, int32_t n_nodes, const int3
     rc = gdnhost::check_tree(parent_host, d->batch, n_nodes, false, 0);
     if (rc != GDN_OK) return rc;
     if (flags & ~(uint32_t)GDN_VERIFY_STATE_READY) return GDN_ERR_FLAGS;
+    if (x_ready && !gdnhost::aligned_to(x_ready, 4)) return GDN_ERR_ALIGN;
     VerifyArgs v = make_args(d, n_nodes - 1, x, a, b, conv_w, ssm_in, conv_in, ssm_ckpt, conv_ckpt, out,
                              parent_dev, dev_status);
     v.early = (flags & GDN_VERIFY_STATE_READY) ? 1 : 0;
+    v.x_ready = x_ready;
     return dispatch_verify<true>(d, v, static_cast<cudaStream_t>(stream));
 }
 

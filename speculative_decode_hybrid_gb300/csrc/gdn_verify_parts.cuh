@@ -43,6 +43,8 @@ struct VerifyArgs {
     int steal;              // work-stealing kernel: ask for pending items (0: every CTA runs its own item)
     int early;              // GDN_VERIFY_STATE_READY: the state, conv taps / state and parents may be
                             // read before the wait for the previous grid on the stream
+    const int32_t *x_ready; // inputs landing during the launch: the x, a, b rows of (request, layer)
+                            // by may be read once x_ready[by] != 0 (null: all there at launch)
 };
 
 // One work item: (request*layer by, value head h, row block rb).
@@ -98,6 +100,7 @@ __device__ __forceinline__ Buf buf_cckpt(const VerifyArgs &p) { return {p.conv_c
 __device__ __forceinline__ Buf buf_out(const VerifyArgs &p) { return {p.out, n_by(p) * p.Tb * p.H_v * p.d_v * 4}; }
 __device__ __forceinline__ Buf buf_parent(const VerifyArgs &p) { return {p.parent, (size_t)p.B * (p.Tb + 1) * 4}; }
 __device__ __forceinline__ Buf buf_accept(const VerifyArgs &p) { return {p.accept_len, (size_t)p.B * 4}; }
+__device__ __forceinline__ Buf buf_ready(const VerifyArgs &p) { return {p.x_ready, (size_t)p.B * p.Y * 4}; }
 
 __host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -188,6 +191,41 @@ __device__ __forceinline__ int steal_result(unsigned resp, unsigned bar, unsigne
         : "l"(lo), "l"(hi)
         : "memory");
     return ok ? x : -1;
+}
+
+// ---------------------------------------------------------------------------
+// Inputs landing during the launch (x_ready non-null): the x, a and b rows of
+// (request, layer) by may be read once x_ready[by] != 0. A copy engine sets
+// the flag after it has copied the rows (the caller's contract: no kernel
+// sets it, since a kernel could wait for an SM that this launch holds). The
+// flag is read with acquire semantics at system scope, so the rows' bytes
+// are visible to the reading thread after it; a warp or block barrier then
+// orders the other threads' reads after that one.
+// ---------------------------------------------------------------------------
+constexpr unsigned kReadyPolls = 1u << 20;  // with the back-off below, about a quarter second
+
+__device__ __forceinline__ bool ready_flag(const VerifyArgs &p, int by) {
+    const int32_t *f = p.x_ready + by;
+    if (!GDN_IN(f, 4, buf_ready(p), p.dev_status)) return true;
+    int v;
+    asm volatile("ld.acquire.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v != 0;
+}
+
+// Wait (bounded) until the rows of by have landed: lane 0 of each calling
+// warp polls, then the warp's barrier. A wait that gives up sets
+// GDN_DEV_SCHED (the item then reads whatever is there).
+__device__ __forceinline__ void wait_ready(const VerifyArgs &p, int by) {
+    if (!p.x_ready) return;
+    if ((threadIdx.x & 31) == 0) {
+        bool ok = false;
+        for (unsigned i = 0; i < kReadyPolls && !ok; ++i) {
+            ok = ready_flag(p, by);
+            if (!ok) __nanosleep(200);
+        }
+        if (!ok && p.dev_status) atomicOr(p.dev_status, GDN_DEV_SCHED);
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ void bar_sync(int id, int count) {
@@ -803,6 +841,7 @@ VerifyArgs make_args(const gdn_dims *d, int32_t T, const void *x, const void *a,
     v.rpi = kRowsPerCta;
     v.steal = 1;
     v.early = 0;
+    v.x_ready = nullptr;
     return v;
 }
 

@@ -53,7 +53,7 @@ EXPORTED = ("gdn_verify_span", "gdn_tree_verify", "spec_accept_greedy",
             "spec_accept_workspace_bytes", "gdn_rollback_restore", "gdn_tree_check",
             "gdn_status_str", "gdn_verify_span_nockpt", "gdn_commit_replay", "spec_topk",
             "spec_topk_workspace_bytes", "gdn_verify_span_wy", "gdn_commit_wy", "gdn_verify_span_ex",
-            "gdn_tree_verify_ex")
+            "gdn_tree_verify_ex", "gdn_verify_span_pipelined", "gdn_tree_verify_pipelined")
 
 
 class GdnError(RuntimeError):
@@ -99,6 +99,8 @@ def load(path: Optional[str] = None):
         u32 = ctypes.c_uint32
         lib.gdn_verify_span_ex.argtypes = [dp, i32] + [vp] * 9 + [vp, u32, vp]
         lib.gdn_tree_verify_ex.argtypes = [dp, i32, vp, vp] + [vp] * 9 + [vp, u32, vp]
+        lib.gdn_verify_span_pipelined.argtypes = [dp, i32] + [vp] * 9 + [vp, u32, vp, vp]
+        lib.gdn_tree_verify_pipelined.argtypes = [dp, i32, vp, vp] + [vp] * 9 + [vp, u32, vp, vp]
         lib.spec_accept_greedy.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         lib.spec_accept_workspace_bytes.argtypes = [i32, i32]
         lib.spec_accept_workspace_bytes.restype = sz
@@ -114,7 +116,7 @@ def load(path: Optional[str] = None):
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
         for f in ("gdn_verify_span", "gdn_tree_verify", "gdn_verify_span_ex", "gdn_tree_verify_ex",
-                  "spec_accept_greedy",
+                  "gdn_verify_span_pipelined", "gdn_tree_verify_pipelined", "spec_accept_greedy",
                   "gdn_rollback_restore", "gdn_tree_check", "gdn_verify_span_nockpt",
                   "gdn_commit_replay", "spec_topk", "gdn_verify_span_wy", "gdn_commit_wy"):
             getattr(lib, f).restype = ctypes.c_int
@@ -157,19 +159,26 @@ def _ok(rc: int, what: str):
 
 
 def gdn_verify_span(dims: gdn_dims, n_tok: int, x, a, b, conv_w, ssm_in, conv_in,
-                    ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None, flags: int = 0) -> None:
-    """gdn_verify_span, or gdn_verify_span_ex when flags (GDN_VERIFY_*) are given."""
+                    ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None, flags: int = 0,
+                    x_ready=None) -> None:
+    """gdn_verify_span; gdn_verify_span_ex when flags (GDN_VERIFY_*) are given;
+    gdn_verify_span_pipelined when x_ready (device int32 [batch][layers]) is."""
     args = (ctypes.byref(dims), int(n_tok), _ptr(x), _ptr(a), _ptr(b), _ptr(conv_w), _ptr(ssm_in),
             _ptr(conv_in), _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out), _ptr(dev_status))
-    if flags:
+    if x_ready is not None:
+        _ok(load().gdn_verify_span_pipelined(*args, int(flags), _ptr(x_ready), _stream(stream)),
+            "gdn_verify_span_pipelined")
+    elif flags:
         _ok(load().gdn_verify_span_ex(*args, int(flags), _stream(stream)), "gdn_verify_span_ex")
     else:
         _ok(load().gdn_verify_span(*args, _stream(stream)), "gdn_verify_span")
 
 
 def gdn_tree_verify(dims: gdn_dims, n_nodes: int, parent_host, parent_dev, x, a, b, conv_w, ssm_in,
-                    conv_in, ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None, flags: int = 0) -> None:
-    """gdn_tree_verify, or gdn_tree_verify_ex when flags (GDN_VERIFY_*) are given."""
+                    conv_in, ssm_ckpt, conv_ckpt, out, dev_status=None, stream=None, flags: int = 0,
+                    x_ready=None) -> None:
+    """gdn_tree_verify; gdn_tree_verify_ex when flags (GDN_VERIFY_*) are given;
+    gdn_tree_verify_pipelined when x_ready (device int32 [batch][layers]) is."""
     import numpy as np
     ph = None
     if parent_host is not None:
@@ -177,7 +186,10 @@ def gdn_tree_verify(dims: gdn_dims, n_nodes: int, parent_host, parent_dev, x, a,
     args = (ctypes.byref(dims), int(n_nodes), _ptr(ph), _ptr(parent_dev), _ptr(x), _ptr(a), _ptr(b),
             _ptr(conv_w), _ptr(ssm_in), _ptr(conv_in), _ptr(ssm_ckpt), _ptr(conv_ckpt), _ptr(out),
             _ptr(dev_status))
-    if flags:
+    if x_ready is not None:
+        _ok(load().gdn_tree_verify_pipelined(*args, int(flags), _ptr(x_ready), _stream(stream)),
+            "gdn_tree_verify_pipelined")
+    elif flags:
         _ok(load().gdn_tree_verify_ex(*args, int(flags), _stream(stream)), "gdn_tree_verify_ex")
     else:
         _ok(load().gdn_tree_verify(*args, _stream(stream)), "gdn_tree_verify")

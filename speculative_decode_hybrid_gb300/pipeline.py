@@ -59,20 +59,27 @@ class SpecStep:
         self.accept_len = self.result[:B]
         self.accept_node = self.result[B:2 * B]
         self.argmax = self.result[2 * B:].view(B, s.n_nodes)
+        # inputs landing during the verify (the pipelined host step): x_ready[b][y]
+        # != 0 once the x, a, b rows of (b, y) are on the device, set from the
+        # pinned ones by the copy that follows those rows
+        self.x_ready = torch.zeros((B, Y), dtype=torch.int32, device=dev)
+        self._ones = torch.ones((B * Y,), dtype=torch.int32).pin_memory()
         self.ws_bytes = G.spec_accept_workspace_bytes(B, s.n_nodes)
         self.workspace = torch.zeros((self.ws_bytes,), dtype=torch.uint8, device=dev)
         self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
 
     # -- the three calls -------------------------------------------------
-    def verify(self, stream=None):
+    def verify(self, stream=None, x_ready=None):
+        """The verify of all requests and layers as one launch; x_ready (device
+        int32 [B][Y]): inputs that land during it (the _pipelined calls)."""
         if self.tree:
             G.gdn_tree_verify(self.dims, self.n_nodes, self.parent_host, self.parent, self.x, self.a,
                               self.b, self.conv_w, self.ssm_state, self.conv_state, self.ssm_ckpt,
-                              self.conv_ckpt, self.out, self.dev_status, stream)
+                              self.conv_ckpt, self.out, self.dev_status, stream, x_ready=x_ready)
         else:
             G.gdn_verify_span(self.dims, self.n_tok, self.x, self.a, self.b, self.conv_w,
                               self.ssm_state, self.conv_state, self.ssm_ckpt, self.conv_ckpt,
-                              self.out, self.dev_status, stream)
+                              self.out, self.dev_status, stream, x_ready=x_ready)
 
     def accept(self, stream=None):
         s = self.shape
@@ -285,24 +292,37 @@ class SpecStep:
             for name in ("accept_len", "accept_node", "argmax"):
                 out_host[name].copy_(getattr(self, name), non_blocking=True)
 
-    def capture_host_step(self, host: dict, out_host: dict, commit: str = "checkpoint", chunks=(1, 3, 8)):
+    def capture_host_step(self, host: dict, out_host: dict, commit: str = "checkpoint", chunks=None,
+                          pipelined=None):
         """Capture the end-to-end step for fixed pinned host buffers (see
         run_host_step) into one CUDA graph that pipelines the host link with
-        the verify:
-        - a copy branch DMAs x, a, b in contiguous blocks in item order
-          (blocks(chunks): layer ranges for one request, request ranges
-          otherwise), then logits, tokens (and parent). The default sizes
-          1 : 3 : 8 expose only a small first copy while each later block
-          lands before the verify needs it (48 layers: 4, 12, 32 layers;
-          this beat 4 equal blocks by 2-4 %, 2 and 5 blocks too);
-        - the verify of each block is its own launch on its own branch, and
-          starts as soon as its block has landed (the blocks' layers and
-          requests are independent), so only the first block's copy is
-          exposed;
-        - all branches join before the acceptance; then come the commit
-          (restore or replay) and the D2H copies of the result.
-        One eager host step runs first, outside the capture."""
+        the verify. A copy branch DMAs x, a, b in contiguous blocks in item
+        order (blocks(chunks): layer ranges for one request, request ranges
+        otherwise), then logits and tokens. Then:
+        - pipelined (the checkpoint commit; the default there): one verify
+          launch starts at once on the main branch (gdn_*_verify_pipelined);
+          after each block the copy branch sets that block's flags in x_ready
+          (a host-to-device copy of ones, queued behind the block's rows), and
+          the kernel waits for an item's flag before it reads the item's x,
+          a, b. A tree's parent array is copied first and the verify waits for
+          it. Default blocks 1 : 1 : 2 : 4 : 8 : 8 (48 layers: 2, 2, 4, 8, 16,
+          16): small first blocks for the verify's first items, larger ones
+          once the copies run ahead of it. x_ready is zeroed after the step;
+        - otherwise (the replay commits, whose kernels take no flags): the
+          verify of each block is its own launch on its own branch, which
+          starts when its block has landed (the blocks' layers and requests
+          are independent); default blocks 1 : 3 : 8 (48 layers: 4, 12, 32;
+          this beat 4 equal blocks by 2-4 %, 2 and 5 blocks too).
+        All branches join before the acceptance; then come the commit
+        (restore or replay) and the D2H copy of the result. One eager host
+        step runs first, outside the capture."""
         finish = {"checkpoint": self.restore, "replay": self.commit_replay, "wy": self.commit_wy}[commit]
+        if pipelined is None:
+            pipelined = commit == "checkpoint"
+        if pipelined and commit != "checkpoint":
+            raise ValueError("the pipelined host step is for the checkpoint commit")
+        if chunks is None:
+            chunks = (1, 1, 2, 4, 8, 8) if pipelined else (1, 3, 8)
         saved = getattr(self, "commit", "checkpoint")
         self.commit = commit
         run_host_step(self, host, out_host)
@@ -312,21 +332,58 @@ class SpecStep:
         g = torch.cuda.CUDAGraph()
         main = torch.cuda.Stream(device=self.device)
         copy = torch.cuda.Stream(device=self.device)
-        branches = [torch.cuda.Stream(device=self.device) for _ in blocks]
         main.wait_stream(torch.cuda.current_stream(self.device))
+        if pipelined:
+            Y = self.shape.layers
+            flat = self.x_ready.view(-1)
+            with torch.cuda.graph(g, stream=main):
+                fork = torch.cuda.Event()
+                fork.record(main)
+                copy.wait_event(fork)
+                parent_done = None
+                with torch.cuda.stream(copy):
+                    if self.tree and "parent" in host:
+                        self.parent.copy_(host["parent"], non_blocking=True)
+                        parent_done = torch.cuda.Event()
+                        parent_done.record(copy)
+                    for b0, b1, y0, y1 in blocks:
+                        for name in ("x", "a", "b"):
+                            getattr(self, name)[b0:b1, y0:y1].copy_(host[name][b0:b1, y0:y1], non_blocking=True)
+                        i0, i1 = b0 * Y + y0, (b1 - 1) * Y + y1  # the block's (request, layer) items
+                        flat[i0:i1].copy_(self._ones[i0:i1], non_blocking=True)
+                    for name in ("logits", "tokens"):
+                        if name in host:
+                            getattr(self, name).copy_(host[name], non_blocking=True)
+                copied = torch.cuda.Event()
+                copied.record(copy)
+                if parent_done is not None:
+                    main.wait_event(parent_done)
+                self.verify(stream=main, x_ready=self.x_ready)
+                main.wait_event(copied)
+                self.accept(stream=main)
+                finish(stream=main)
+                self.x_ready.zero_()  # for the next step's copies
+                self._copy_result(out_host)
+            torch.cuda.current_stream(self.device).wait_stream(main)
+            self._graph_host = g
+            self._graph_host_bufs = (host, out_host)
+            return g
+        branches = [torch.cuda.Stream(device=self.device) for _ in blocks]
         with torch.cuda.graph(g, stream=main):
             fork = torch.cuda.Event()
             fork.record(main)
             copy.wait_event(fork)
             landed = []
             with torch.cuda.stream(copy):
+                if "parent" in host:  # first: every block's tree verify reads it
+                    self.parent.copy_(host["parent"], non_blocking=True)
                 for b0, b1, y0, y1 in blocks:
                     for name in ("x", "a", "b"):
                         getattr(self, name)[b0:b1, y0:y1].copy_(host[name][b0:b1, y0:y1], non_blocking=True)
                     e = torch.cuda.Event()
                     e.record(copy)
                     landed.append(e)
-                for name in ("logits", "tokens", "parent"):
+                for name in ("logits", "tokens"):
                     if name in host:
                         getattr(self, name).copy_(host[name], non_blocking=True)
             copied = torch.cuda.Event()
