@@ -445,9 +445,14 @@ def run_e2e(args, st, wl, flush, dev, stream, K, units, ws, kl):
     mode = "eager copies + device graph"
     try:
         st.capture_host_step(host, out_host, args.commit)
-        mode = "one graph per step: x/a/b copied in 3 blocks (sizes 1:3:8), the verify of each block " \
-               "launched as its block lands, logits/tokens copied during the verify, then accept, " \
-               "commit, D2H of the result"
+        if args.commit == "checkpoint":
+            mode = "one graph per step: one verify launch at once (gdn_*_verify_pipelined) while x/a/b land " \
+                   "in blocks (sizes 1:1:2:4:8:8), each block's flags set by a copy behind it; " \
+                   "logits/tokens copied during the verify, then accept, commit, one D2H of the result"
+        else:
+            mode = "one graph per step: x/a/b copied in 3 blocks (sizes 1:3:8), the verify of each block " \
+                   "launched as its block lands, logits/tokens copied during the verify, then accept, " \
+                   "commit, one D2H of the result"
     except Exception as exc:  # capture unsupported: copies stay eager around the device graph
         print("host-step capture failed: %r" % (exc,), file=sys.stderr)
     for i in range(E + 3):
