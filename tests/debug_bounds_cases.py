@@ -85,6 +85,30 @@ def main():
     for st, what in ((a, "step"), (b, "replay"), (c, "wy")):
         assert status(st) == 0, (what, status(st))
 
+    # the pipelined verify calls (flags set up front; batch 16 takes the
+    # work-stealing path) and the pipelined end-to-end step graph, whose
+    # copies set the flags while the verify runs
+    from speculative_decode_hybrid_gb300.pipeline import pinned_host_inputs, run_host_step
+    for wid, layers in ((2, 3), (3, 3), (4, 1)):
+        wl = W.make_workload(wid, seed=9 + wid, layers=layers)
+        a, b = SpecStep(wl), SpecStep(wl)
+        a.verify()
+        b.x_ready.fill_(1)
+        b.verify(x_ready=b.x_ready)
+        torch.cuda.synchronize()
+        assert torch.equal(a.out, b.out) and torch.equal(a.ssm_ckpt, b.ssm_ckpt), ("pipelined", wid)
+        assert status(b) == 0, ("pipelined", wid, status(b))
+        if wid == 4:
+            continue
+        st = SpecStep(wl)
+        out = st.host_result_buffers()
+        host = pinned_host_inputs(wl)
+        st.capture_host_step(host, out, "checkpoint")
+        for _ in range(2):
+            run_host_step(st, host, out, graph=True)
+        torch.cuda.synchronize()
+        assert status(st) == 0, ("pipelined host step", wid, status(st))
+
     # top-k and the no-allocation accept
     g = np.random.default_rng(11)
     for rows, V, k in ((3, 151936, 32), (5, 1001, 7), (1, 64, 1)):
