@@ -292,8 +292,15 @@ __device__ __forceinline__ void recurrence(const VerifyArgs &p, RowState<DK, SL>
             const int root_slot = plan_s[p.T];
             if (root_slot >= 0) park_rows(rs, tmem, root_slot);  // the item's initial loads have landed by now
         }
+        // each node's order and plan entries are read one node ahead, before
+        // the stores of the node in hand
+        int node_n = p.T > 0 ? ord_s[0] : 0, pl_n = p.T > 0 ? plan_s[0] : 0;
         for (int q = 0; q < p.T; ++q) {
-            const int node = ord_s[q], pl = plan_s[q];
+            const int node = node_n, pl = pl_n;
+            if (q + 1 < p.T) {
+                node_n = ord_s[q + 1];
+                pl_n = plan_s[q + 1];
+            }
             const int src = (int)(short)(pl & 0xffff), park = pl >> 16;
             if (src >= 0) {
                 if constexpr (PARK) fetch_rows(rs, tmem, src);
