@@ -238,3 +238,26 @@ def test_verify_ex_validates_flags_before_launch(lib):
     bad = np.array([-1, 0, 3, 1], dtype=np.int32)
     assert lib.gdn_tree_verify_ex(ctypes.byref(d), 4, bad.ctypes.data, *args, FAKE, None,
                                   G.GDN_VERIFY_STATE_READY, None) == G.GDN_ERR_TREE_PARENT
+
+
+def test_pipelined_verify_validates_before_launch(lib):
+    """The _pipelined calls check what the _ex calls check, plus the input-flag
+    array's alignment (GDN_ERR_ALIGN), before anything is queued; with a null
+    x_ready they are the _ex calls."""
+    d = _dims()
+    args = [FAKE] * 9
+    odd = ctypes.c_void_p(FAKE + 2)  # not 4-byte aligned
+    assert lib.gdn_verify_span_pipelined(ctypes.byref(d), 4, *args, None, 0, odd, None) == G.GDN_ERR_ALIGN
+    assert lib.gdn_verify_span_pipelined(ctypes.byref(d), 4, *args, None, 0x2, FAKE, None) == G.GDN_ERR_FLAGS
+    assert lib.gdn_verify_span_pipelined(ctypes.byref(d), 0, *args, None, 0, FAKE, None) == G.GDN_ERR_DIMS
+    assert lib.gdn_verify_span_pipelined(None, 4, *args, None, 0, FAKE, None) == G.GDN_ERR_NULL
+    bad_x = [None] + [FAKE] * 8  # x missing
+    assert lib.gdn_verify_span_pipelined(ctypes.byref(d), 4, *bad_x, None, 0, FAKE, None) == G.GDN_ERR_NULL
+    par = np.array([-1, 0, 1, 1], dtype=np.int32)
+    assert lib.gdn_tree_verify_pipelined(ctypes.byref(d), 4, par.ctypes.data, *args, FAKE, None, 0, odd,
+                                         None) == G.GDN_ERR_ALIGN
+    assert lib.gdn_tree_verify_pipelined(ctypes.byref(d), 4, par.ctypes.data, *args, FAKE, None, 0x4, FAKE,
+                                         None) == G.GDN_ERR_FLAGS
+    bad = np.array([-1, 0, 3, 1], dtype=np.int32)
+    assert lib.gdn_tree_verify_pipelined(ctypes.byref(d), 4, bad.ctypes.data, *args, FAKE, None, 0, FAKE,
+                                         None) == G.GDN_ERR_TREE_PARENT
