@@ -512,19 +512,20 @@ def test_host_buffer_step_matches_device_step():
     np.testing.assert_array_equal(packed["argmax"][0].numpy(), am)
 
 
-@pytest.mark.parametrize("wid,commit", [(2, "checkpoint"), (3, "checkpoint"), (2, "replay"), (2, "wy")])
+@pytest.mark.parametrize("wid,commit", [(2, "checkpoint"), (3, "checkpoint"), (4, "checkpoint"), (2, "replay"),
+                                        (2, "wy")])
 def test_host_step_graph_equals_eager_host_steps(wid, commit):
     """The whole host step as one graph (copies on two branches, the step,
     the read-back) gives the eager host step's bytes, step after step."""
     from speculative_decode_hybrid_gb300.pipeline import pinned_host_inputs, run_host_step
     wl = W.make_workload(wid, seed=9, layers=2)
-    N = wl.shape.n_nodes
+    N, B = wl.shape.n_nodes, wl.shape.batch
     host = pinned_host_inputs(wl)
 
     def outs():
-        return {"accept_len": torch.empty(1, dtype=torch.int32).pin_memory(),
-                "accept_node": torch.empty(1, dtype=torch.int32).pin_memory(),
-                "argmax": torch.empty((1, N), dtype=torch.int32).pin_memory()}
+        return {"accept_len": torch.empty(B, dtype=torch.int32).pin_memory(),
+                "accept_node": torch.empty(B, dtype=torch.int32).pin_memory(),
+                "argmax": torch.empty((B, N), dtype=torch.int32).pin_memory()}
 
     eager, graph = SpecStep(wl), SpecStep(wl)
     eager.commit = commit
