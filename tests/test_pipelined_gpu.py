@@ -93,3 +93,36 @@ def test_pipelined_wait_gives_up_on_a_flag_nothing_sets():
     torch.cuda.synchronize()
     _same(a, b)
     assert int(b.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_pipelined_on_the_fallback_kernel(tree):
+    """An x that is not 16-byte aligned takes the one-item-per-CTA kernel, whose
+    CTAs wait for their item's flag at entry: with the rows and flags landing
+    behind a long copy, the same bytes as the plain call (which runs the
+    staged kernel on an aligned x)."""
+    wl = W.make_workload(3 if tree else 2, seed=36, layers=3)
+    ref = SpecStep(wl)
+    ref.verify()
+    st = SpecStep(wl)
+    host = {n: getattr(st, n).cpu().pin_memory() for n in ("x", "a", "b")}
+    shifted = torch.empty(st.x.numel() + 8, dtype=st.x.dtype, device="cuda")
+    st.x = shifted[1:1 + st.x.numel()].view(st.x.shape)  # a 2-byte offset
+    assert st.x.data_ptr() % 16 != 0
+    for n in ("x", "a", "b"):
+        getattr(st, n).zero_()
+    ballast_h = torch.empty(64 << 20, dtype=torch.uint8).pin_memory()
+    ballast_d = torch.empty_like(ballast_h, device="cuda")
+    torch.cuda.synchronize()
+    copy = torch.cuda.Stream()
+    with torch.cuda.stream(copy):
+        ballast_d.copy_(ballast_h, non_blocking=True)
+        Y = wl.shape.layers
+        for y in range(Y):
+            for n in ("x", "a", "b"):
+                getattr(st, n)[0, y].copy_(host[n][0, y], non_blocking=True)
+            st.x_ready.view(-1)[y:y + 1].copy_(st._ones[y:y + 1], non_blocking=True)
+    st.verify(stream=torch.cuda.current_stream(), x_ready=st.x_ready)
+    torch.cuda.synchronize()
+    _same(ref, st)
+    assert int(st.dev_status.item()) == 0
